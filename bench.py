@@ -1,0 +1,444 @@
+"""Benchmark of libfnorm on GB300: effective HBM GB/s (algorithmic bytes: read
+x once, write y once) and the fraction of the measured HBM peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra]
+
+One step is one call of the hot path over one batch of the workload. The
+default workload is InstanceNorm2d forward, fp32, x[112,64,512,512] ~ N(0,1)
+(7168 slices of 512x512; 7.5 GB read, 7.5 GB written). The input is larger
+than L2, so no flush is needed between steps. Under torchrun each rank runs
+its own copy of the workload on its own GPU (weak scaling; the slices are
+independent, so there is no collective) and the time is the max over ranks.
+
+``--impl reference`` times the CPU oracle (single-threaded, float64) on a
+bounded sample of the same workload on the host cores.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import normalization_reduction_gb300 as fn  # noqa: E402
+from normalization_reduction_gb300 import inputs  # noqa: E402
+
+METRIC = "effective HBM GB/s (min bytes/time) and % of GB300 peak per normalization config"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+L2_BYTES = 126 * 1024 * 1024
+
+# DRAM bytes (read + write) per launch of each workload's dominant kernel from
+# one ncu capture (profiles/*.md); None until measured for the current kernel.
+NCU_TRAFFIC = {}
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ workloads
+class Workload:
+    name = ""
+    launches = 1          # our kernel launches per step
+    dtype = "f32"
+    kernel = ""
+
+    def bytes_per_step(self) -> int:
+        raise NotImplementedError
+
+    def step(self, stream):
+        raise NotImplementedError
+
+
+class InstanceNormLarge(Workload):
+    name = "instancenorm2d_fp32_112x64x512x512"
+    kernel = "in_resident_kernel"
+
+    def __init__(self, dev, shape=inputs.SHAPE_LARGE):
+        self.shape = shape
+        self.x = inputs.instancenorm_large(dev, shape)
+        self.y = torch.empty_like(self.x)
+        self.N, self.C = shape[0], shape[1]
+        self.S = shape[2] * shape[3]
+
+    def bytes_per_step(self):
+        return self.x.numel() * 8
+
+    def step(self, stream):
+        fn.fnorm_instancenorm(self.x, self.y, self.N, self.C, self.S, fn.FNORM_F32, fn.FNORM_F32,
+                              1e-5, None, None, stream)
+
+
+class Epilogue(Workload):
+    name = "epilogue_fp32_128x16x14x30x30"
+    kernel = "epi_resident_kernel"
+
+    def __init__(self, dev, copies=None):
+        x, m = inputs.epilogue(dev)
+        self.N, self.C = x.shape[0], x.shape[1]
+        self.S = x[0, 0].numel()
+        nbytes = x.numel() * 4
+        copies = copies or max(1, -(-4 * L2_BYTES // nbytes))   # rotate >= 4x L2
+        self.xs = [x] + [x.clone() for _ in range(copies - 1)]
+        self.ys = [torch.empty((self.N, self.S), device=dev) for _ in range(copies)]
+        self.m = m
+        self.i = 0
+
+    def bytes_per_step(self):
+        return self.N * self.C * self.S * 4 + self.N * self.S * 4 + self.C * 4
+
+    def step(self, stream):
+        k = self.i % len(self.xs)
+        self.i += 1
+        fn.fnorm_instancenorm_epilogue(self.xs[k], self.m, self.ys[k], None, self.N, self.C,
+                                       self.S, 1e-5, -1.0, 1.0, stream)
+
+
+class BatchNorm(Workload):
+    name = "batchnorm2d_train_fp32_128x64x126x126"
+    kernel = "bn_apply_kernel"
+    launches = 3
+
+    def __init__(self, dev):
+        self.x, self.g, self.b, self.rm, self.rv = inputs.batchnorm(dev)
+        self.y = torch.empty_like(self.x)
+        self.N, self.C = self.x.shape[0], self.x.shape[1]
+        self.S = self.x[0, 0].numel()
+        nb = fn.fnorm_batchnorm_workspace_size(self.N, self.C, self.S)
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+    def bytes_per_step(self):
+        return self.x.numel() * 8
+
+    def step(self, stream):
+        fn.fnorm_batchnorm_train(self.x, self.y, self.g, self.b, 2.0, self.rm, self.rv, 0.1, 1e-5,
+                                 None, None, self.N, self.C, self.S, self.ws, self.ws.numel(),
+                                 stream)
+
+
+class Sweep(Workload):
+    kernel = "in_*_kernel"
+    dtype = "bf16"
+
+    def __init__(self, dev, S):
+        self.name = f"instancenorm_bf16_sweep_S{S}"
+        self.x = inputs.instancenorm_sweep(S, dev)
+        self.y = torch.empty_like(self.x)
+        self.N, self.C, self.S = self.x.shape
+
+    def bytes_per_step(self):
+        return self.x.numel() * 4
+
+    def step(self, stream):
+        fn.fnorm_instancenorm(self.x, self.y, self.N, self.C, self.S, fn.FNORM_BF16, fn.FNORM_BF16,
+                              1e-5, None, None, stream)
+
+
+# ------------------------------------------------------------------ timing
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.proc = None
+        self.dev = dev_index
+
+    def __enter__(self):
+        try:
+            ident = str(self.dev)
+            try:
+                u = torch.cuda.get_device_properties(self.dev).uuid
+                ident = "GPU-" + str(u)
+            except Exception:
+                pass
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_workload(wl: Workload, steps: int, warmup: int, ws: int, sample_clocks=False):
+    """Device time per step (ms) with CUDA events on the launching stream."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if sample_clocks else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    start.record(stream)
+    for i in range(steps):
+        per[i][0].record(stream)
+        wl.step(stream)
+        per[i][1].record(stream)
+    end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    barrier(ws)
+    if sampler:
+        sampler.__exit__()
+    total_ms = start.elapsed_time(end)
+    step_ms = [a.elapsed_time(b) for a, b in per]
+    return total_ms, step_ms, (sampler.summary() if sampler else None)
+
+
+def e2e_instancenorm(wl: InstanceNormLarge, steps: int, chunk_slices: int = 448):
+    """Same metric through the C ABI with the input and output in pinned HOST
+    memory: every step copies x host->device, normalises, copies y back.
+    Chunks of slices go round-robin over three streams so copies overlap the
+    kernel and each other."""
+    NC = wl.N * wl.C
+    S = wl.S
+    xh = torch.empty((NC, S), dtype=torch.float32, pin_memory=True)
+    yh = torch.empty((NC, S), dtype=torch.float32, pin_memory=True)
+    xh.copy_(wl.x.view(NC, S)[:NC])
+    dx = wl.x.view(NC, S)
+    dy = wl.y.view(NC, S)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    chunks = [(a, min(NC, a + chunk_slices)) for a in range(0, NC, chunk_slices)]
+
+    def one_step():
+        for i, (a, b) in enumerate(chunks):
+            s = streams[i % len(streams)]
+            with torch.cuda.stream(s):
+                dx[a:b].copy_(xh[a:b], non_blocking=True)
+                fn.fnorm_instancenorm(dx[a:b], dy[a:b], 1, b - a, S, fn.FNORM_F32, fn.FNORM_F32,
+                                      1e-5, None, None, s)
+                yh[a:b].copy_(dy[a:b], non_blocking=True)
+
+    one_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    nbytes = NC * S * 4
+    return {"value": round(wl.bytes_per_step() / dt / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(dt * 1e3, 3), "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes, "pipeline": f"{len(chunks)} chunks over 3 streams"}
+
+
+def cpu_baseline(x_dev: torch.Tensor, S: int, budget_s: float = 10.0, batch: int = 256):
+    """The oracle on a bounded sample of the workload's slices (host cores)."""
+    import oracle
+    orc = oracle.get()
+    NC = x_dev.numel() // S
+    xv = x_dev.view(NC, S)
+    done = 0
+    elapsed = 0.0
+    while done < NC and elapsed < budget_s:
+        b = min(batch, NC - done)
+        xs = xv[done:done + b].cpu().numpy()
+        t0 = time.perf_counter()
+        orc.instancenorm(xs)
+        elapsed += time.perf_counter() - t0
+        done += b
+    nbytes = done * S * 8
+    return {"value": round(nbytes / elapsed / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{done} of {NC} slices ({done * S} elements), float64 single-threaded"}
+
+
+def run_ours(args):
+    ws, rank, local = dist_info()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peak, peak_kind = peak_hbm()
+
+    wl = InstanceNormLarge(dev)
+    total_ms, step_ms, clocks = time_workload(wl, args.steps, args.warmup, ws, sample_clocks=True)
+    total_ms = max_over_ranks(total_ms, ws)
+    ms = total_ms / args.steps
+    nbytes = wl.bytes_per_step()
+    value = nbytes * ws / (ms * 1e-3) / 1e9
+    kernel_ms = statistics.mean(step_ms)
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1), generated on device)",
+        "config": {"workload": wl.name, "shape": list(wl.shape), "eps": 1e-5,
+                   "bytes_per_step": nbytes, "l2": "input larger than L2 (7.5 GB), no flush",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "pct_of_peak": round(100 * value / ws / peak, 2),
+        "pct_of_nominal": round(100 * value / ws / NOMINAL_HBM_GBS, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": NCU_TRAFFIC.get(wl.name), "peak_source": peak_kind,
+                     "kernel": wl.kernel},
+        "gpu_launches": wl.launches * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_extra:
+        res["e2e"] = e2e_instancenorm(wl, max(2, min(args.steps, 5)))
+        res["cpu_baseline"] = cpu_baseline(wl.x, wl.S)
+    del wl
+    torch.cuda.empty_cache()
+    if not args.no_extra:
+        res["per_config"] = other_configs(dev, ws, peak)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def other_configs(dev, ws, peak):
+    """The other workloads, same timing rules (reported alongside)."""
+    out = {}
+    cases = [("epilogue", lambda: Epilogue(dev), 200, 20),
+             ("batchnorm", lambda: BatchNorm(dev), 20, 5)]
+    cases += [(f"sweep_S{S}", (lambda S=S: Sweep(dev, S)), 10, 3) for S in inputs.SWEEP_S]
+    for key, make, steps, warm in cases:
+        wl = make()
+        total_ms, step_ms, _ = time_workload(wl, steps, warm, ws)
+        ms = max_over_ranks(total_ms, ws) / steps
+        gbs = wl.bytes_per_step() / (ms * 1e-3) / 1e9
+        out[key] = {"workload": wl.name, "ms_per_step": round(ms, 4), "GB/s": round(gbs, 1),
+                    "pct_of_peak": round(100 * gbs / peak, 2), "launches_per_step": wl.launches}
+        if isinstance(wl, BatchNorm):
+            out[key]["GB/s_two_read_basis"] = round(gbs * 1.5, 1)
+        del wl
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    orc = oracle.get()
+    shape = inputs.SHAPE_LARGE
+    S = shape[2] * shape[3]
+    NC = shape[0] * shape[1]
+    sample = 24   # slices per step: a bounded sample of the workload
+    x = inputs.normal((sample, S), inputs.SEED_LARGE, "cpu").numpy()
+    for _ in range(args.warmup):
+        orc.instancenorm(x)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        orc.instancenorm(x)
+        times.append(time.perf_counter() - t0)
+    per = statistics.mean(times)
+    gbs = sample * S * 8 / per / 1e9
+    res = {"impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+           "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+           "config": {"workload": "instancenorm2d_fp32_112x64x512x512", "shape": list(shape),
+                      "sample_slices_per_step": sample, "of_slices": NC},
+           "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": f"{sample} of {NC} slices per step, float64 single-threaded"},
+           "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    del np
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip e2e, cpu baseline and the other workloads")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

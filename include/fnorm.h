@@ -1,0 +1,168 @@
+/*
+ * fnorm.h -- libfnorm: normalisation with per-slice statistics on NVIDIA
+ * GB300 (sm_103a), as a C ABI.
+ *
+ * Sources (web pages; titles as on the pages, each page a sequence of
+ * reasoning blocks counted from 1):
+ *   Kimi-K2.6__l1_p34  InstanceNorm2d(64) on x[112,64,512,512].
+ *   Kimi-K2.6__l2_p79  Conv3d -> x*m_c -> InstanceNorm3d -> clamp[-1,1]
+ *                      -> x*m_c -> max over channels.
+ *   Kimi-K2.6__l2_p73  Conv2d -> BatchNorm2d (training) -> x*2.0.
+ * The convolutions that precede these steps on the pages are not part of
+ * this library: callers pass the convolution's output.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are contiguous, row-major, with the slice (spatial) axis
+ *    innermost: x is [N][C][S] where S is the product of the spatial sizes.
+ *  - Pointers named x, y, m, gamma, ... are DEVICE pointers owned by the
+ *    caller. The library allocates no memory of its own.
+ *  - Calls are asynchronous and ordered on `stream` (NULL = the legacy
+ *    default stream). A returned FNORM_OK means the work was validated and
+ *    enqueued; execution errors surface at the caller's next synchronisation.
+ *  - Argument errors are returned before anything is launched and leave every
+ *    output untouched. No C++ exception crosses this interface.
+ *  - Element counts use 64-bit indices throughout (N*C*S may exceed 2^31).
+ *  - N*C == 0 or S == 0 is a no-op that returns FNORM_OK.
+ *  - Results are deterministic: the same inputs give bitwise-identical
+ *    outputs (all reductions combine partial results in a fixed order).
+ *  - Statistics: the mean and the biased variance (divide by the element
+ *    count) over each slice, combined across threads, CTAs and clusters with
+ *    the Chan/Welford pairwise update; normalisation is
+ *    (x - mean) * rsqrt(var + eps) computed in fp32.
+ *  - Fast paths need x and y 16-byte aligned and the slice length a multiple
+ *    of one 16-byte vector; other (element-aligned) inputs take a scalar-load
+ *    path with the same results. Pointers not aligned to their element size
+ *    are rejected with FNORM_ERR_ALIGNMENT.
+ */
+#ifndef FNORM_H
+#define FNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FNORM_API __attribute__((visibility("default")))
+#else
+#define FNORM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fnorm_stream_t;
+
+typedef enum fnorm_status {
+  FNORM_OK = 0,
+  FNORM_ERR_INVALID_ARG = 1, /* bad size, null pointer, bad eps, overlapping buffers */
+  FNORM_ERR_UNSUPPORTED = 2, /* valid request this build cannot serve (e.g. dtype combination) */
+  FNORM_ERR_ALIGNMENT = 3,   /* pointer not aligned to its element size */
+  FNORM_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  FNORM_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (see fnorm_get_last_error) */
+} fnorm_status;
+
+typedef enum fnorm_dtype {
+  FNORM_F32 = 0, /* IEEE binary32 */
+  FNORM_BF16 = 1 /* bfloat16; computed in fp32, stored with round-to-nearest-even */
+} fnorm_dtype;
+
+/*
+ * InstanceNorm forward, affine = False (Kimi-K2.6__l1_p34, blocks 1-2: the
+ * per-(n,c) mean and biased variance over the H*W plane, then
+ * (x - mean)/sqrt(var + eps) with eps = 1e-5 by default).
+ *
+ *   x         [N*C][S] input of type in_dtype.
+ *   y         [N*C][S] output of type out_dtype. y may equal x (in place);
+ *             any other overlap is rejected.
+ *   eps       >= 0 (finite). With eps = 0 a constant slice yields NaN.
+ *   mean_out  optional [N*C] fp32: the slice means (NULL to skip).
+ *   rstd_out  optional [N*C] fp32: 1/sqrt(var + eps) (NULL to skip).
+ * Every (in_dtype, out_dtype) pair of F32/BF16 is supported.
+ * A slice is read from HBM once and written once whenever it fits in one
+ * thread-block cluster (up to 2 MiB of input per slice); longer slices are
+ * read twice (statistics pass, then normalisation pass).
+ */
+FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
+                                fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                float* mean_out, float* rstd_out, fnorm_stream_t stream);
+
+/*
+ * Fused post-convolution epilogue (Kimi-K2.6__l2_p79, block 1: the pipeline
+ * scaled = conv_out*m, InstanceNorm over the spatial extent, clamp, a second
+ * multiply by m, then the max over the channel dimension), fp32:
+ *
+ *   v      = x[n,c,s] * m[c]
+ *   t      = (v - mean_nc(v)) / sqrt(var_nc(v) + eps)
+ *   y[n,s] = max over c of  m[c] * clamp(t, clamp_lo, clamp_hi)
+ *
+ *   x       [N][C][S] fp32.       m [C] fp32.       y [N][S] fp32.
+ *   argmax  optional [N][S] int64: the channel index of the maximum, the
+ *           lowest index among equal maxima (NULL to skip).
+ *   clamp   clamp_lo <= clamp_hi; clamp(t) = min(max(t, lo), hi).
+ * y and argmax must not overlap x, m or each other.
+ * When a sample's C slices fit on chip in one cluster (C*S*4 bytes up to
+ * about 3 MiB) x is read once; otherwise each slice is read twice.
+ */
+FNORM_API fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
+                                         int64_t N, int64_t C, int64_t S, float eps,
+                                         float clamp_lo, float clamp_hi, fnorm_stream_t stream);
+
+/*
+ * Bytes of device workspace fnorm_batchnorm_train needs for this shape
+ * (a multiple of 256; 0 when N*C*S == 0).
+ */
+FNORM_API size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S);
+
+/*
+ * Training-mode BatchNorm forward with a trailing scale factor
+ * (Kimi-K2.6__l2_p73, blocks 1-2: BatchNorm2d in training mode followed by
+ * x*scaling_factor; running statistics update with momentum, the running
+ * variance taking the unbiased estimate as Kimi-K2.6__l2_p79 block 1 states):
+ *
+ *   per channel c over all (n, s): mean_c, var_c (biased), n_c = N*S
+ *   y = scale * (gamma_c * (x - mean_c) * rsqrt(var_c + eps) + beta_c)
+ *   running_mean_c <- (1 - momentum) * running_mean_c + momentum * mean_c
+ *   running_var_c  <- (1 - momentum) * running_var_c
+ *                     + momentum * var_c * n_c / (n_c - 1)
+ *
+ *   x, y          [N][C][S] fp32; y may equal x (in place).
+ *   gamma, beta   optional [C] fp32 (NULL means 1 and 0).
+ *   running_mean, running_var  optional [C] fp32, updated in place
+ *                 (NULL: not updated). Both or neither.
+ *   save_mean, save_rstd  optional [C] fp32: mean_c and rsqrt(var_c + eps).
+ *   workspace     device memory of at least
+ *                 fnorm_batchnorm_workspace_size(N, C, S) bytes, 256-byte
+ *                 aligned, owned by the caller; its contents need no
+ *                 initialisation and are overwritten. Calls that overlap in
+ *                 time must not share a workspace.
+ * Requires N*S >= 2 (the unbiased estimate needs two values).
+ * x is read twice (statistics, then normalisation in reverse order so that
+ * the tail of the first pass is still in L2) and y written once.
+ */
+FNORM_API fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma, const float* beta,
+                                   float scale, float* running_mean, float* running_var,
+                                   float momentum, float eps, float* save_mean, float* save_rstd,
+                                   int64_t N, int64_t C, int64_t S, void* workspace,
+                                   size_t workspace_bytes, fnorm_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+FNORM_API const char* fnorm_status_string(fnorm_status status);
+
+/*
+ * Reads and clears the device error word of the current device: the first
+ * device-side failure (a bounded wait that expired) recorded by any kernel
+ * since the last call. Synchronises the current device first. Returns
+ * FNORM_OK when nothing was recorded, FNORM_ERR_TIMEOUT after an expired
+ * wait, FNORM_ERR_CUDA if the word could not be read.
+ */
+FNORM_API fnorm_status fnorm_get_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch. */
+FNORM_API int fnorm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FNORM_H */

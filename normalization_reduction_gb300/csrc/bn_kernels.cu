@@ -1,0 +1,164 @@
+// bn_kernels.cu -- training-mode BatchNorm forward with a trailing scale
+// (page Kimi-K2.6__l2_p73, blocks 1-2: BatchNorm2d in training mode, batch
+// statistics per channel over (N, H, W), affine gamma/beta, then
+// x * scaling_factor; the running statistics are updated with momentum, the
+// running variance from the unbiased estimate as page Kimi-K2.6__l2_p79,
+// block 1, states).
+//
+// A channel's values are N runs of S contiguous elements, C*S apart. A channel
+// of the page's tensor (128 x 126 x 126 fp32 = 8.1 MB) is far larger than any
+// on-chip store, so x is read twice:
+//   1. bn_stats_kernel   -- one CTA per (run, chunk of <= 16384 elements):
+//                           128-bit loads, exact two-pass per 16-value register
+//                           tile, Chan merges -> one partial (n, mean, M2) per
+//                           CTA in the caller's workspace;
+//   2. bn_finalize_kernel -- one CTA per channel merges its partials in index
+//                           order (deterministic), writes (mean, A, B) with
+//                           y = (x - mean)*A + B, A = scale*gamma*rstd,
+//                           B = scale*beta, the saved statistics and the
+//                           running-statistic update;
+//   3. bn_apply_kernel   -- the normalisation pass, visiting runs in the
+//                           reverse of the statistics pass so the last ~100 MB
+//                           read by pass 1 are still in L2.
+#include "fnorm_device.cuh"
+#include "fnorm_internal.h"
+#include "in_kernels.cuh"
+
+namespace fnorm {
+
+// Thread-level statistics of elements [lo, hi) of run xr in tiles of
+// THREADS*U*4 elements (vector mode: lo and the run length are multiples of 4).
+template <int THREADS, int U, bool VEC>
+__device__ __forceinline__ Stat bn_range_stat(const float* xr, int64_t lo, int64_t hi) {
+  Stat acc = stat_empty();
+  const int tid = threadIdx.x;
+  constexpr int64_t TILE = static_cast<int64_t>(THREADS) * U * 4;
+  for (int64_t t = lo; t < hi; t += TILE) {
+    uint4 r[U];
+    int nvalid;
+    if (VEC) {
+      const int64_t v0 = t / 4 + tid, vend = hi / 4;
+      nvalid = v0 < vend ? clamp_int((vend - v0 + THREADS - 1) / THREADS, 0, U) * 4 : 0;
+      const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
+#pragma unroll
+      for (int k = 0; k < U; ++k) r[k] = (k * 4 < nvalid) ? ld_v4(xv + k * THREADS) : make_uint4(0, 0, 0, 0);
+    } else {
+      const int64_t e0 = t + tid;
+      nvalid = e0 < hi ? clamp_int((hi - e0 + THREADS - 1) / THREADS, 0, U * 4) : 0;
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        r[k] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (k * 4 + j < nvalid)
+            Elem<float>::set(r[k], j, __ldg(xr + e0 + static_cast<int64_t>(k * 4 + j) * THREADS));
+      }
+    }
+    acc = chan_merge(acc, tile_stat<float, U>(r, nvalid));
+  }
+  return acc;
+}
+
+template <int THREADS, int U, bool VEC>
+__global__ void __launch_bounds__(THREADS) bn_stats_kernel(const BnParams p) {
+  __shared__ Stat warp_part[THREADS / 32];
+  const int64_t c = blockIdx.y, b = blockIdx.x;
+  const int64_t n = b / p.chunks, k = b - n * p.chunks;
+  const float* xr = p.x + (n * p.C + c) * p.S;
+  const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
+  const Stat cta = cta_merge<THREADS>(bn_range_stat<THREADS, U, VEC>(xr, lo, hi), warp_part);
+  if (threadIdx.x == 0)
+    p.partials[c * (p.N * p.chunks) + b] = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+}
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) bn_finalize_kernel(const BnParams p) {
+  __shared__ Stat warp_part[THREADS / 32];
+  const int64_t c = blockIdx.x;
+  const int64_t P = p.N * p.chunks;
+  const float4* part = p.partials + c * P;
+  Stat acc = stat_empty();
+  for (int64_t i = threadIdx.x; i < P; i += THREADS) {
+    const float4 v = part[i];
+    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
+  }
+  const Stat s = cta_merge<THREADS>(acc, warp_part);
+  if (threadIdx.x == 0) {
+    const float var = s.m2 / s.n;
+    const float rstd = rsqrtf(var + p.eps);
+    const float g = p.gamma ? p.gamma[c] : 1.f;
+    const float bt = p.beta ? p.beta[c] : 0.f;
+    p.coef[c] = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
+    if (p.save_mean) p.save_mean[c] = s.mean;
+    if (p.save_rstd) p.save_rstd[c] = rstd;
+    if (p.running_mean && p.running_var) {
+      const double cnt = static_cast<double>(p.N) * static_cast<double>(p.S);
+      const double mom = p.momentum;
+      const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
+      p.running_mean[c] =
+          static_cast<float>((1.0 - mom) * p.running_mean[c] + mom * static_cast<double>(s.mean));
+      p.running_var[c] = static_cast<float>((1.0 - mom) * p.running_var[c] + mom * unbiased);
+    }
+  }
+}
+
+template <int THREADS, int U, bool VEC>
+__global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
+  // reverse of the statistics pass's block order
+  const int64_t nb = static_cast<int64_t>(gridDim.x);
+  const int64_t lin = static_cast<int64_t>(gridDim.y) * nb - 1 -
+                      (static_cast<int64_t>(blockIdx.y) * nb + blockIdx.x);
+  const int64_t c = lin / nb, b = lin - c * nb;
+  const int64_t n = b / p.chunks, k = b - n * p.chunks;
+  const int64_t off = (n * p.C + c) * p.S;
+  const float* xr = p.x + off;
+  float* yr = p.y + off;
+  const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
+  const float4 cf = p.coef[c];
+  const int tid = threadIdx.x;
+  constexpr int64_t TILE = static_cast<int64_t>(THREADS) * U * 4;
+  const int64_t ntiles = (hi - lo + TILE - 1) / TILE;
+  for (int64_t ti = ntiles - 1; ti >= 0; --ti) {
+    const int64_t t = lo + ti * TILE;
+    if (VEC) {
+      const int64_t v0 = t / 4 + tid, vend = hi / 4;
+      const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
+      float* yv = yr + v0 * 4;
+      uint4 r[U];
+#pragma unroll
+      for (int k2 = 0; k2 < U; ++k2)
+        if (v0 + k2 * THREADS < vend) r[k2] = ld_v4(xv + k2 * THREADS);
+#pragma unroll
+      for (int k2 = 0; k2 < U; ++k2) {
+        if (v0 + k2 * THREADS < vend) {
+          float o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[j] = fmaf(Elem<float>::get(r[k2], j) - cf.x, cf.y, cf.z);
+          VecStore<float, 4>::run(yv + static_cast<int64_t>(k2) * THREADS * 4, o);
+        }
+      }
+    } else {
+      for (int64_t e = t + tid; e < t + TILE && e < hi; e += THREADS)
+        yr[e] = fmaf(__ldg(xr + e) - cf.x, cf.y, cf.z);
+    }
+  }
+}
+
+template <bool VEC>
+static cudaError_t bn_launch_t(const BnParams& p, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
+  bn_stats_kernel<kBnThreads, kBnUnroll, VEC><<<grid, kBnThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bn_finalize_kernel<kBnThreads><<<static_cast<unsigned>(p.C), kBnThreads, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bn_apply_kernel<kBnThreads, kBnUnroll, VEC><<<grid, kBnThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t bn_launch(const BnParams& p, cudaStream_t stream) {
+  return p.vec ? bn_launch_t<true>(p, stream) : bn_launch_t<false>(p, stream);
+}
+
+}  // namespace fnorm

@@ -1,0 +1,517 @@
+// fnorm_api.cu -- the libfnorm C ABI: argument validation, choice of kernel
+// and launch shape, stream-ordered launches, status codes and the device
+// error word. Declarations and contracts are in include/fnorm.h.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+
+#include "../../include/fnorm.h"
+#include "fnorm_internal.h"
+
+namespace fnorm {
+
+// Device error word: kernels OR failure codes into it (bounded waits that
+// expired); fnorm_get_last_error reads and clears it. One instance per device.
+__device__ unsigned int g_fnorm_err_word;
+
+namespace {
+
+std::mutex g_mutex;
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_valid[kMaxDevices];
+unsigned* g_err_ptr[kMaxDevices];
+std::map<std::string, int> g_occupancy;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return d;
+}
+
+// Device address of this device's error word (looked up once per device with
+// that device current).
+unsigned* err_word() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (!g_err_ptr[d]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fnorm_err_word) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_err_ptr[d] = static_cast<unsigned*>(ptr);
+  }
+  return g_err_ptr[d];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [a, a+na) and [b, b+nb) share a byte (empty ranges never overlap).
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  return !__builtin_mul_overflow(a, b, out) && *out <= (int64_t(1) << 56);
+}
+
+bool finite_nonneg(float v) { return std::isfinite(v) && v >= 0.f; }
+
+const char* env(const char* name) {
+  const char* v = std::getenv(name);
+  return (v && *v) ? v : nullptr;
+}
+
+int occupancy_cached(const std::string& key, int (*query)(const void*), const void* arg) {
+  const int d = current_device();
+  const std::string k = std::to_string(d) + "|" + key;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    auto it = g_occupancy.find(k);
+    if (it != g_occupancy.end()) return it->second;
+  }
+  const int v = query(arg);
+  std::lock_guard<std::mutex> lk(g_mutex);
+  g_occupancy[k] = v;
+  return v;
+}
+
+fnorm_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FNORM_OK;
+  cudaGetLastError();
+  return FNORM_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ InstanceNorm
+struct InCall {
+  int tin, tout;   // 0 = f32, 1 = bf16
+  InPlan plan;
+};
+
+cudaError_t in_launch_dispatch(int tin, int tout, const InParams& p, const InPlan& plan,
+                               cudaStream_t s) {
+  if (tin == 0 && tout == 0) return in_launch_t<float, float>(p, plan, s);
+  if (tin == 0 && tout == 1) return in_launch_t<float, __nv_bfloat16>(p, plan, s);
+  if (tin == 1 && tout == 1) return in_launch_t<__nv_bfloat16, __nv_bfloat16>(p, plan, s);
+  return in_launch_t<__nv_bfloat16, float>(p, plan, s);
+}
+
+struct InQuery {
+  int tin, tout;
+  InPlan plan;
+};
+
+int in_query(const void* arg) {
+  const InQuery& q = *static_cast<const InQuery*>(arg);
+  if (q.tin == 0 && q.tout == 0) return in_max_active_clusters_t<float, float>(q.plan);
+  if (q.tin == 0 && q.tout == 1) return in_max_active_clusters_t<float, __nv_bfloat16>(q.plan);
+  if (q.tin == 1 && q.tout == 1)
+    return in_max_active_clusters_t<__nv_bfloat16, __nv_bfloat16>(q.plan);
+  return in_max_active_clusters_t<__nv_bfloat16, float>(q.plan);
+}
+
+int in_capacity(int tin, int tout, const InPlan& plan) {
+  char key[128];
+  std::snprintf(key, sizeof key, "in|%d|%d|%d|%d|%d|%d|%d|%d", tin, tout,
+                static_cast<int>(plan.path), plan.vec ? 1 : 0, plan.threads, plan.nv, plan.group,
+                plan.cluster);
+  InQuery q{tin, tout, plan};
+  return occupancy_cached(key, in_query, &q);
+}
+
+// Parses FNORM_FORCE_PATH (test and tuning hook):
+//   group:G:NV | resident:THREADS:NV:CLUSTER | stream:CLUSTER
+bool in_forced_plan(InPlan* plan) {
+  const char* f = env("FNORM_FORCE_PATH");
+  if (!f) return false;
+  int a = 0, b = 0, c = 0;
+  if (std::sscanf(f, "group:%d:%d", &a, &b) == 2) {
+    plan->path = InPath::kGroup;
+    plan->group = a;
+    plan->nv = b;
+    plan->threads = 256;
+    plan->cluster = 1;
+    return true;
+  }
+  if (std::sscanf(f, "resident:%d:%d:%d", &a, &b, &c) == 3) {
+    plan->path = InPath::kResident;
+    plan->threads = a;
+    plan->nv = b;
+    plan->cluster = c;
+    return true;
+  }
+  if (std::sscanf(f, "stream:%d", &a) == 1) {
+    plan->path = InPath::kStream;
+    plan->threads = kStreamThreads;
+    plan->nv = kStreamUnroll;
+    plan->cluster = a;
+    return true;
+  }
+  return false;
+}
+
+// Chooses the kernel and launch shape for an InstanceNorm call.
+fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64_t NC, int64_t S,
+                          InPlan* out) {
+  const int es_in = tin == 0 ? 4 : 2, es_out = tout == 0 ? 4 : 2;
+  const int W = 16 / es_in;
+  const size_t out_vec_bytes = static_cast<size_t>(W) * es_out;
+  InPlan plan{};
+  plan.vec = aligned(x, 16) && aligned(y, out_vec_bytes < 16 ? out_vec_bytes : 16) && S % W == 0 &&
+             !env("FNORM_FORCE_SCALAR");
+  const int64_t slots = (S + W - 1) / W;
+
+  if (in_forced_plan(&plan)) {
+    int64_t cap = 0;
+    if (plan.path == InPath::kGroup) cap = int64_t(plan.group) * plan.nv;
+    if (plan.path == InPath::kResident) cap = int64_t(plan.threads) * plan.nv * plan.cluster;
+    if (plan.path == InPath::kStream) cap = slots;
+    if (cap < slots || plan.cluster < 1 || plan.cluster > kMaxCluster) return FNORM_ERR_UNSUPPORTED;
+  } else if (slots <= 256) {
+    plan.path = InPath::kGroup;
+    plan.threads = 256;
+    plan.cluster = 1;
+    for (const auto& g : kGroupShapes) {
+      if (int64_t(g[0]) * g[1] >= slots) {
+        plan.group = g[0];
+        plan.nv = g[1];
+        break;
+      }
+    }
+  } else if (slots <= int64_t(kMaxCluster) * 8192) {
+    plan.path = InPath::kResident;
+    if (slots <= 8192) {
+      plan.cluster = 1;
+      for (const auto& r : kResidentShapes) {
+        if (int64_t(r[0]) * r[1] >= slots) {
+          plan.threads = r[0];
+          plan.nv = r[1];
+          break;
+        }
+      }
+    } else {
+      // Wide slices: CTA shape (threads x 8 slots) and cluster size. The CTA
+      // shape is tunable through FNORM_RESIDENT_THREADS (512 or 1024).
+      const char* t = env("FNORM_RESIDENT_THREADS");
+      plan.threads = (t && std::atoi(t) == 512) ? 512 : 1024;
+      plan.nv = 8;
+      const int64_t per = int64_t(plan.threads) * plan.nv;
+      plan.cluster = static_cast<int>((slots + per - 1) / per);
+      if (plan.cluster > kMaxCluster) {
+        plan.threads = 1024;
+        plan.cluster = static_cast<int>((slots + 8191) / 8192);
+      }
+    }
+  } else {
+    plan.path = InPath::kStream;
+    plan.threads = kStreamThreads;
+    plan.nv = kStreamUnroll;
+    plan.cluster = 8;
+  }
+
+  int cap = in_capacity(tin, tout, plan);
+  if (cap <= 0 && plan.path != InPath::kGroup && plan.cluster > 8 && !env("FNORM_FORCE_PATH")) {
+    // 16-CTA clusters not available: stream the slice with a portable cluster.
+    plan.path = InPath::kStream;
+    plan.threads = kStreamThreads;
+    plan.nv = kStreamUnroll;
+    plan.cluster = 8;
+    cap = in_capacity(tin, tout, plan);
+  }
+  if (cap <= 0) return FNORM_ERR_UNSUPPORTED;
+
+  if (plan.path == InPath::kGroup) {
+    const int64_t per_block = int64_t(8) * (32 / plan.group);
+    const int64_t need = (NC + per_block - 1) / per_block;
+    plan.grid = static_cast<int>(need < cap ? need : cap);
+  } else {
+    const int64_t clusters = NC < cap ? NC : cap;
+    plan.grid = static_cast<int>(clusters * plan.cluster);
+  }
+  *out = plan;
+  return FNORM_OK;
+}
+
+// ------------------------------------------------------------ Epilogue
+struct EpiQuery {
+  EpiPlan plan;
+};
+int epi_query(const void* arg) { return epi_max_active_clusters(static_cast<const EpiQuery*>(arg)->plan); }
+
+int epi_capacity(const EpiPlan& plan) {
+  char key[128];
+  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%zu", static_cast<int>(plan.path), plan.threads,
+                plan.cluster, plan.smem);
+  EpiQuery q{plan};
+  return occupancy_cached(key, epi_query, &q);
+}
+
+constexpr size_t kEpiTargetBytes = 110 * 1024;   // per-CTA share of a sample, 2 CTAs per SM
+
+fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax, int64_t N,
+                           int64_t C, int64_t S, EpiPlan* out) {
+  const DeviceInfo& di = device_info();
+  const bool vec = aligned(x, 16) && aligned(y, 16) && (!argmax || aligned(argmax, 16)) &&
+                   S % 4 == 0 && !env("FNORM_EPI_STREAM");
+  const char* force_cl = env("FNORM_EPI_CLUSTER");
+  EpiPlan plan{};
+  plan.threads = kEpiThreads;
+  bool have = false;
+  if (vec) {
+    const int cands[] = {1, 2, 4, 8, 16};
+    int chosen = 0;
+    for (int pass = 0; pass < 2 && !chosen; ++pass) {
+      for (int cl : cands) {
+        if (force_cl && cl != std::atoi(force_cl)) continue;
+        const int64_t cpc = (C + cl - 1) / cl;
+        const size_t smem = epi_resident_smem(C, S, static_cast<int>(cpc));
+        const size_t bytes = static_cast<size_t>(cpc) * S * 4;
+        if (smem > static_cast<size_t>(di.max_smem_optin) || bytes >= (size_t(1) << 20)) continue;
+        if (pass == 0 && !force_cl && bytes > kEpiTargetBytes) continue;
+        EpiPlan cand{EpiPath::kResident, kEpiThreads, static_cast<int>((C + cpc - 1) / cpc),
+                     static_cast<int>(cpc), smem, 0};
+        if (cand.cluster < 1) cand.cluster = 1;
+        if (epi_capacity(cand) > 0) {
+          plan = cand;
+          chosen = cl;
+          break;
+        }
+      }
+    }
+    have = chosen != 0;
+  }
+  if (!have) {
+    plan.path = EpiPath::kStream;
+    plan.cluster = kEpiStreamCluster;
+    plan.cpc = 0;
+    plan.smem = epi_stream_smem(C, plan.cluster);
+    if (plan.smem > static_cast<size_t>(di.max_smem_optin)) return FNORM_ERR_UNSUPPORTED;
+  }
+  const int cap = epi_capacity(plan);
+  if (cap <= 0) return FNORM_ERR_UNSUPPORTED;
+  const int64_t clusters = N < cap ? N : cap;
+  plan.grid = static_cast<int>(clusters * plan.cluster);
+  *out = plan;
+  return FNORM_OK;
+}
+
+// ------------------------------------------------------------ BatchNorm
+struct BnLayout {
+  int64_t chunk, chunks, P;
+  size_t part_bytes, coef_bytes;
+};
+
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+BnLayout bn_layout(int64_t N, int64_t C, int64_t S) {
+  BnLayout l{};
+  l.chunk = kBnChunk;
+  l.chunks = S > 0 ? (S + l.chunk - 1) / l.chunk : 0;
+  l.P = N * l.chunks;
+  l.part_bytes = round256(static_cast<size_t>(C) * l.P * 16);
+  l.coef_bytes = round256(static_cast<size_t>(C) * 16);
+  return l;
+}
+
+}  // namespace
+
+const DeviceInfo& device_info() {
+  static DeviceInfo fallback{1, 48 * 1024, 0};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return fallback;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (!g_info_valid[d]) {
+    DeviceInfo di{};
+    cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, d);
+    cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    cudaDeviceGetAttribute(&di.cluster_launch, cudaDevAttrClusterLaunch, d);
+    cudaGetLastError();
+    g_info[d] = di;
+    g_info_valid[d] = true;
+  }
+  return g_info[d];
+}
+
+}  // namespace fnorm
+
+using namespace fnorm;
+
+extern "C" {
+
+int fnorm_version(void) { return 100; }
+
+const char* fnorm_status_string(fnorm_status s) {
+  switch (s) {
+    case FNORM_OK: return "FNORM_OK";
+    case FNORM_ERR_INVALID_ARG: return "FNORM_ERR_INVALID_ARG";
+    case FNORM_ERR_UNSUPPORTED: return "FNORM_ERR_UNSUPPORTED";
+    case FNORM_ERR_ALIGNMENT: return "FNORM_ERR_ALIGNMENT";
+    case FNORM_ERR_CUDA: return "FNORM_ERR_CUDA";
+    case FNORM_ERR_TIMEOUT: return "FNORM_ERR_TIMEOUT";
+  }
+  return "FNORM_ERR_UNKNOWN";
+}
+
+fnorm_status fnorm_get_last_error(void) {
+  unsigned* w = err_word();
+  if (!w) return FNORM_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fnorm_err_word, sizeof v) != cudaSuccess)
+    return cuda_status(cudaErrorUnknown);
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_fnorm_err_word, &zero, sizeof zero) != cudaSuccess)
+    return cuda_status(cudaErrorUnknown);
+  return (v & kErrTimeout) ? FNORM_ERR_TIMEOUT : FNORM_OK;
+}
+
+fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
+                                fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                float* mean_out, float* rstd_out, fnorm_stream_t stream) {
+  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if ((in_dtype != FNORM_F32 && in_dtype != FNORM_BF16) ||
+      (out_dtype != FNORM_F32 && out_dtype != FNORM_BF16))
+    return FNORM_ERR_INVALID_ARG;
+  if (!finite_nonneg(eps)) return FNORM_ERR_INVALID_ARG;
+  int64_t NC = 0, total = 0;
+  if (!mul_ok(N, C, &NC) || !mul_ok(NC, S, &total)) return FNORM_ERR_INVALID_ARG;
+  if (total == 0) return FNORM_OK;
+  if (!x || !y) return FNORM_ERR_INVALID_ARG;
+  const int tin = in_dtype == FNORM_F32 ? 0 : 1, tout = out_dtype == FNORM_F32 ? 0 : 1;
+  const size_t es_in = tin == 0 ? 4 : 2, es_out = tout == 0 ? 4 : 2;
+  if (!aligned(x, es_in) || !aligned(y, es_out) || (mean_out && !aligned(mean_out, 4)) ||
+      (rstd_out && !aligned(rstd_out, 4)))
+    return FNORM_ERR_ALIGNMENT;
+  const size_t xb = static_cast<size_t>(total) * es_in, yb = static_cast<size_t>(total) * es_out;
+  if (x != y && overlaps(x, xb, y, yb)) return FNORM_ERR_INVALID_ARG;
+  if (x == y && es_in != es_out) return FNORM_ERR_INVALID_ARG;
+  const size_t sb = static_cast<size_t>(NC) * 4;
+  if (overlaps(mean_out, sb, x, xb) || overlaps(mean_out, sb, y, yb) ||
+      overlaps(rstd_out, sb, x, xb) || overlaps(rstd_out, sb, y, yb) ||
+      overlaps(mean_out, sb, rstd_out, sb))
+    return FNORM_ERR_INVALID_ARG;
+
+  InPlan plan;
+  fnorm_status st = in_make_plan(tin, tout, x, y, NC, S, &plan);
+  if (st != FNORM_OK) return st;
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  const InParams p{x, y, NC, S, eps, mean_out, rstd_out, err};
+  return cuda_status(in_launch_dispatch(tin, tout, p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
+                                         int64_t N, int64_t C, int64_t S, float eps,
+                                         float clamp_lo, float clamp_hi, fnorm_stream_t stream) {
+  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if (!finite_nonneg(eps) || std::isnan(clamp_lo) || std::isnan(clamp_hi) || !(clamp_lo <= clamp_hi))
+    return FNORM_ERR_INVALID_ARG;
+  int64_t NS = 0, NC = 0, total = 0;
+  if (!mul_ok(N, S, &NS) || !mul_ok(N, C, &NC) || !mul_ok(NC, S, &total))
+    return FNORM_ERR_INVALID_ARG;
+  if (NS == 0) return FNORM_OK;
+  if (C == 0) return FNORM_ERR_INVALID_ARG;   // a max over no channels is undefined
+  if (C > kEpiMaxChannels) return FNORM_ERR_UNSUPPORTED;
+  if (!x || !m || !y) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(m, 4) || !aligned(y, 4) || (argmax && !aligned(argmax, 8)))
+    return FNORM_ERR_ALIGNMENT;
+  const size_t xb = static_cast<size_t>(total) * 4, yb = static_cast<size_t>(NS) * 4,
+               ab = argmax ? static_cast<size_t>(NS) * 8 : 0, mb = static_cast<size_t>(C) * 4;
+  if (overlaps(y, yb, x, xb) || overlaps(y, yb, m, mb) || overlaps(argmax, ab, x, xb) ||
+      overlaps(argmax, ab, m, mb) || overlaps(argmax, ab, y, yb))
+    return FNORM_ERR_INVALID_ARG;
+
+  EpiPlan plan;
+  fnorm_status st = epi_make_plan(x, y, argmax, N, C, S, &plan);
+  if (st != FNORM_OK) return st;
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  EpiParams p{x, m, y, argmax, N, C, S, eps, clamp_lo, clamp_hi, plan.cpc,
+              (env("FNORM_DEBUG_FORCE_TIMEOUT") && plan.path == EpiPath::kResident) ? 1 : 0, err};
+  return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S) {
+  if (N <= 0 || C <= 0 || S <= 0) return 0;
+  int64_t t1 = 0, t2 = 0;
+  if (!mul_ok(N, C, &t1) || !mul_ok(t1, S, &t2)) return 0;
+  const BnLayout l = bn_layout(N, C, S);
+  return l.part_bytes + l.coef_bytes;
+}
+
+fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma, const float* beta,
+                                   float scale, float* running_mean, float* running_var,
+                                   float momentum, float eps, float* save_mean, float* save_rstd,
+                                   int64_t N, int64_t C, int64_t S, void* workspace,
+                                   size_t workspace_bytes, fnorm_stream_t stream) {
+  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if (!finite_nonneg(eps) || !std::isfinite(scale) || !std::isfinite(momentum))
+    return FNORM_ERR_INVALID_ARG;
+  if ((running_mean == nullptr) != (running_var == nullptr)) return FNORM_ERR_INVALID_ARG;
+  int64_t NC = 0, total = 0, NS = 0;
+  if (!mul_ok(N, C, &NC) || !mul_ok(NC, S, &total) || !mul_ok(N, S, &NS))
+    return FNORM_ERR_INVALID_ARG;
+  if (total == 0) return FNORM_OK;
+  if (NS < 2) return FNORM_ERR_INVALID_ARG;   // the unbiased estimate needs two values
+  if (C > 65535) return FNORM_ERR_UNSUPPORTED;
+  if (!x || !y || !workspace) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256) ||
+      (gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4)) ||
+      (running_mean && !aligned(running_mean, 4)) || (running_var && !aligned(running_var, 4)) ||
+      (save_mean && !aligned(save_mean, 4)) || (save_rstd && !aligned(save_rstd, 4)))
+    return FNORM_ERR_ALIGNMENT;
+  const BnLayout l = bn_layout(N, C, S);
+  if (l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
+  if (workspace_bytes < l.part_bytes + l.coef_bytes) return FNORM_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(total) * 4, cb = static_cast<size_t>(C) * 4,
+               wb = l.part_bytes + l.coef_bytes;
+  if (x != y && overlaps(x, xb, y, xb)) return FNORM_ERR_INVALID_ARG;
+  const void* outs[] = {running_mean, running_var, save_mean, save_rstd};
+  for (const void* o : outs) {
+    if (overlaps(o, cb, x, xb) || overlaps(o, cb, y, xb) || overlaps(o, cb, workspace, wb))
+      return FNORM_ERR_INVALID_ARG;
+  }
+  if (overlaps(workspace, wb, x, xb) || overlaps(workspace, wb, y, xb)) return FNORM_ERR_INVALID_ARG;
+
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  BnParams p{};
+  p.x = x;
+  p.y = y;
+  p.gamma = gamma;
+  p.beta = beta;
+  p.scale = scale;
+  p.running_mean = running_mean;
+  p.running_var = running_var;
+  p.momentum = momentum;
+  p.eps = eps;
+  p.save_mean = save_mean;
+  p.save_rstd = save_rstd;
+  p.N = N;
+  p.C = C;
+  p.S = S;
+  p.chunk = l.chunk;
+  p.chunks = l.chunks;
+  p.partials = static_cast<float4*>(workspace);
+  p.coef = reinterpret_cast<float4*>(static_cast<char*>(workspace) + l.part_bytes);
+  p.vec = aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_SCALAR");
+  p.err = err;
+  return cuda_status(bn_launch(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+// fnorm_internal.h -- host-side contract between the C ABI (fnorm_api.cu)
+// and the kernel translation units: parameter blocks, launch plans and the
+// launcher entry points each kernel file defines.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fnorm {
+
+// Device error word codes (kernels OR them into the word the host passes in).
+constexpr unsigned kErrTimeout = 1u;
+
+// ---------------------------------------------------------------- InstanceNorm
+struct InParams {
+  const void* x;
+  void* y;
+  int64_t NC;
+  int64_t S;
+  float eps;
+  float* mean_out;
+  float* rstd_out;
+  unsigned* err;
+};
+
+enum class InPath : int {
+  kGroup = 0,     // G lanes per slice, slice held in registers (short slices)
+  kResident = 1,  // one CTA or one cluster of CTAs per slice, slice held in registers
+  kStream = 2,    // one cluster per slice, two reads (statistics, then normalise)
+};
+
+struct InPlan {
+  InPath path;
+  bool vec;      // 16-byte vector access (else element-wise)
+  int threads;   // CTA size
+  int nv;        // 16-byte slots per thread (group / resident)
+  int group;     // lanes per slice (group path)
+  int cluster;   // CTAs per slice (resident / stream); 1 = no cluster
+  int grid;      // CTAs to launch (0: the launcher sizes the persistent grid)
+};
+
+// Launch plans the kernel files provide, listed so the dispatcher can choose
+// among them: resident (threads, nv) and group (group, nv) shapes.
+constexpr int kResidentShapes[][2] = {{128, 4}, {256, 4}, {256, 8}, {512, 8}, {1024, 8}};
+constexpr int kGroupShapes[][2] = {{8, 1}, {8, 4}, {32, 2}, {32, 4}, {32, 8}};
+constexpr int kStreamThreads = 512;
+constexpr int kStreamUnroll = 4;
+constexpr int kMaxCluster = 16;
+
+// Defined in in_kernels.cuh and instantiated per (Tin, Tout) in in_*.cu.
+// in_launch_t returns the launch's error code; in_max_active_clusters_t the
+// largest number of co-resident clusters (CTAs for cluster size 1) of the plan
+// on the current device, 0 if the plan cannot run.
+template <class Tin, class Tout>
+cudaError_t in_launch_t(const InParams& p, const InPlan& plan, cudaStream_t stream);
+template <class Tin, class Tout>
+int in_max_active_clusters_t(const InPlan& plan);
+
+// ---------------------------------------------------------------- Epilogue
+struct EpiParams {
+  const float* x;
+  const float* m;
+  float* y;
+  int64_t* argmax;
+  int64_t N;
+  int64_t C;
+  int64_t S;
+  float eps;
+  float lo;
+  float hi;
+  int cpc;             // channels held per CTA (resident path)
+  int debug_timeout;   // test hook: wait on an mbarrier nobody completes
+  unsigned* err;
+};
+
+enum class EpiPath : int { kResident = 0, kStream = 1 };
+
+struct EpiPlan {
+  EpiPath path;
+  int threads;
+  int cluster;
+  int cpc;
+  size_t smem;   // dynamic shared memory bytes
+  int grid;      // CTAs (multiple of cluster)
+};
+
+constexpr int kEpiThreads = 256;
+constexpr int kEpiStreamCluster = 8;
+constexpr int kEpiMaxChannels = 8192;
+
+cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t stream);
+int epi_max_active_clusters(const EpiPlan& plan);
+size_t epi_resident_smem(int64_t C, int64_t S, int cpc);
+size_t epi_stream_smem(int64_t C, int cluster);
+
+// ---------------------------------------------------------------- BatchNorm
+struct BnParams {
+  const float* x;
+  float* y;
+  const float* gamma;
+  const float* beta;
+  float scale;
+  float* running_mean;
+  float* running_var;
+  float momentum;
+  float eps;
+  float* save_mean;
+  float* save_rstd;
+  int64_t N;
+  int64_t C;
+  int64_t S;
+  int64_t chunk;        // elements of one (n,c) run one CTA reduces
+  int64_t chunks;       // chunks per run
+  float4* partials;     // [C][N*chunks] (count, mean, M2, -)
+  float4* coef;         // [C] (mean, A, B, -) with y = (x - mean)*A + B
+  bool vec;
+  unsigned* err;
+};
+
+constexpr int kBnThreads = 256;
+constexpr int kBnUnroll = 4;
+constexpr int64_t kBnChunk = 16384;   // elements per CTA in the two streaming passes
+
+cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- helpers
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;
+  int cluster_launch;
+};
+const DeviceInfo& device_info();   // current device, cached
+
+}  // namespace fnorm

@@ -1,0 +1,124 @@
+"""The C ABI on the CPU: the library loads, exports every declared entry
+point, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import normalization_reduction_gb300 as fn
+from normalization_reduction_gb300 import build as nbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "fnorm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nbuild.build()
+    return fn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fnorm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("fnorm_instancenorm", "fnorm_instancenorm_epilogue",
+                     "fnorm_batchnorm_train", "fnorm_batchnorm_workspace_size",
+                     "fnorm_status_string", "fnorm_get_last_error", "fnorm_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(lib):
+    for s in fn.Status:
+        assert fn.fnorm_status_string(int(s)) == "FNORM_" + s.name
+    assert fn.fnorm_version() >= 100
+
+
+def _rc(call):
+    try:
+        call()
+    except fn.FnormError as e:
+        return e.status
+    return fn.Status.OK
+
+
+FAKE = 1 << 40   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(N=-1), fn.Status.ERR_INVALID_ARG),
+    (dict(eps=-1e-5), fn.Status.ERR_INVALID_ARG),
+    (dict(eps=float("nan")), fn.Status.ERR_INVALID_ARG),
+    (dict(eps=float("inf")), fn.Status.ERR_INVALID_ARG),
+    (dict(in_dtype=7), fn.Status.ERR_INVALID_ARG),
+    (dict(x=0), fn.Status.ERR_INVALID_ARG),
+    (dict(x=FAKE + 2), fn.Status.ERR_ALIGNMENT),
+    (dict(y=FAKE + 4, x=FAKE), fn.Status.ERR_INVALID_ARG),     # partial overlap
+    (dict(y=FAKE, x=FAKE, out_dtype=fn.FNORM_BF16), fn.Status.ERR_INVALID_ARG),
+    (dict(N=0), fn.Status.OK),                                  # empty: no-op
+    (dict(S=0), fn.Status.OK),
+    (dict(N=1 << 40, C=1 << 40), fn.Status.ERR_INVALID_ARG),   # size overflow
+    (dict(mean_out=FAKE + 64, x=FAKE), fn.Status.ERR_INVALID_ARG),
+])
+def test_instancenorm_validation(lib, kw, expect):
+    a = dict(x=FAKE, y=FAKE + (1 << 30), N=2, C=3, S=64, in_dtype=fn.FNORM_F32,
+             out_dtype=fn.FNORM_F32, eps=1e-5, mean_out=None, rstd_out=None, stream=0)
+    a.update(kw)
+    assert _rc(lambda: fn.fnorm_instancenorm(**a)) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(C=0), fn.Status.ERR_INVALID_ARG),
+    (dict(C=9000), fn.Status.ERR_UNSUPPORTED),
+    (dict(clamp_lo=1.0, clamp_hi=-1.0), fn.Status.ERR_INVALID_ARG),
+    (dict(clamp_lo=float("nan")), fn.Status.ERR_INVALID_ARG),
+    (dict(m=0), fn.Status.ERR_INVALID_ARG),
+    (dict(argmax=FAKE + (1 << 30) + 4), fn.Status.ERR_ALIGNMENT),
+    (dict(y=FAKE + 128), fn.Status.ERR_INVALID_ARG),           # y inside x
+    (dict(N=0), fn.Status.OK),
+])
+def test_epilogue_validation(lib, kw, expect):
+    a = dict(x=FAKE, m=FAKE + (1 << 32), y=FAKE + (1 << 30), argmax=None, N=2, C=4, S=64,
+             eps=1e-5, clamp_lo=-1.0, clamp_hi=1.0, stream=0)
+    a.update(kw)
+    assert _rc(lambda: fn.fnorm_instancenorm_epilogue(**a)) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(N=1, S=1), fn.Status.ERR_INVALID_ARG),                # needs two values per channel
+    (dict(workspace_bytes=16), fn.Status.ERR_INVALID_ARG),
+    (dict(workspace=FAKE + (1 << 34) + 16), fn.Status.ERR_ALIGNMENT),
+    (dict(running_var=None), fn.Status.ERR_INVALID_ARG),       # both or neither
+    (dict(momentum=float("nan")), fn.Status.ERR_INVALID_ARG),
+    (dict(C=70000), fn.Status.ERR_UNSUPPORTED),
+    (dict(workspace=FAKE + 256), fn.Status.ERR_INVALID_ARG),   # workspace inside x
+    (dict(C=0), fn.Status.OK),
+])
+def test_batchnorm_validation(lib, kw, expect):
+    a = dict(x=FAKE, y=FAKE + (1 << 30), gamma=None, beta=None, scale=2.0,
+             running_mean=FAKE + (1 << 33), running_var=FAKE + (1 << 33) + 4096, momentum=0.1,
+             eps=1e-5, save_mean=None, save_rstd=None, N=2, C=3, S=64,
+             workspace=FAKE + (1 << 34), workspace_bytes=1 << 20, stream=0)
+    a.update(kw)
+    if "workspace_bytes" not in kw:
+        a["workspace_bytes"] = max(fn.fnorm_batchnorm_workspace_size(a["N"], a["C"], a["S"]), 1 << 20)
+    assert _rc(lambda: fn.fnorm_batchnorm_train(**a)) == expect
+
+
+def test_workspace_size(lib):
+    assert fn.fnorm_batchnorm_workspace_size(0, 4, 4) == 0
+    w = fn.fnorm_batchnorm_workspace_size(128, 64, 126 * 126)
+    assert w % 256 == 0 and w >= 64 * 128 * 16 + 64 * 16
+    # one partial per (run, chunk of up to 16384 elements)
+    assert fn.fnorm_batchnorm_workspace_size(2, 3, 40000) >= 3 * 2 * 3 * 16

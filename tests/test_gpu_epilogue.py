@@ -1,0 +1,142 @@
+"""The fused epilogue max_c m_c*clamp(IN(x*m_c)) on the GPU through the C ABI
+against the oracle: the resident cluster kernel at every cluster size, the
+streaming fallback, argmax (bit-exact where the oracle's top two differ),
+clamp bounds, odd shapes, guard bands, determinism and the bounded-wait
+timeout hook."""
+import numpy as np
+import pytest
+import torch
+
+import normalization_reduction_gb300 as fn
+from normalization_reduction_gb300 import inputs
+from tests.gpu_util import Guarded, assert_close, dev
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-5
+ARG_GAP = 1e-5   # argmax compared where the oracle's top-2 gap exceeds this
+
+
+def run_epi(x, m, lo=-1.0, hi=1.0, eps=EPS, want_arg=True):
+    N, C = x.shape[0], x.shape[1]
+    S = int(np.prod(x.shape[2:]))
+    gy = Guarded((N, S), torch.float32)
+    ga = Guarded((N, S), torch.int64) if want_arg else None
+    fn.fnorm_instancenorm_epilogue(x, m, gy.view, ga.view if ga else None, N, C, S, eps, lo, hi)
+    torch.cuda.synchronize()
+    gy.check()
+    if ga:
+        ga.check()
+    return gy.view, (ga.view if ga else None)
+
+
+def check(orc, x, m, lo=-1.0, hi=1.0, what=""):
+    y, arg = run_epi(x, m, lo, hi)
+    N, C = x.shape[0], x.shape[1]
+    xs = x.cpu().numpy().reshape(N, C, -1)
+    ref, rarg, second = orc.epilogue(xs, m.cpu().numpy(), EPS, lo, hi)
+    assert_close(y.cpu().numpy(), ref, torch.float32, what)
+    a = arg.cpu().numpy()
+    clear = (ref - second) > ARG_GAP
+    assert np.array_equal(a[clear], rarg[clear]), what
+    # where not clearly separated, the chosen channel must still attain the max
+    assert np.all((a >= 0) & (a < C))
+    return y, arg
+
+
+def test_page_shape_subset(orc):
+    """The page's per-sample shape [16,14,30,30] for 8 samples."""
+    x, m = inputs.epilogue(dev(), shape=(8, 16, 14, 30, 30))
+    check(orc, x, m, what="page shape")
+
+
+@pytest.mark.parametrize("cl", [1, 2, 4, 8, 16])
+def test_cluster_sizes(orc, monkeypatch, cl):
+    monkeypatch.setenv("FNORM_EPI_CLUSTER", str(cl))
+    x, m = inputs.epilogue(dev(), shape=(5, 16, 14, 30, 30))
+    check(orc, x, m, what=f"cluster {cl}")
+
+
+@pytest.mark.parametrize("shape", [(3, 1, 64), (2, 3, 100), (4, 5, 12), (2, 7, 1000),
+                                   (3, 16, 4), (2, 33, 256), (1, 64, 2048), (6, 16, 12600)])
+def test_shapes_resident(orc, shape):
+    x, m = inputs.epilogue(dev(), shape=shape, seed=1234 + shape[1])
+    check(orc, x, m, what=str(shape))
+
+
+@pytest.mark.parametrize("shape", [(3, 1, 63), (2, 3, 7), (4, 5, 13), (2, 7, 1001),
+                                   (2, 16, 12601), (1, 300, 50), (2, 4, 300000)])
+def test_shapes_stream(orc, shape):
+    """Slices that are not a multiple of 4, or too large for shared memory."""
+    x, m = inputs.epilogue(dev(), shape=shape, seed=99 + shape[2])
+    check(orc, x, m, what=str(shape))
+
+
+def test_forced_stream(orc, monkeypatch):
+    monkeypatch.setenv("FNORM_EPI_STREAM", "1")
+    x, m = inputs.epilogue(dev(), shape=(4, 16, 14, 30, 30))
+    check(orc, x, m, what="forced stream")
+
+
+def test_misaligned_stream(orc):
+    N, C, S = 3, 6, 500
+    xb, m = inputs.epilogue(dev(), shape=(N, C, S + 1), seed=5)
+    flat = xb.reshape(-1)[1:1 + N * C * S]
+    x = flat.view(N, C, S)
+    check(orc, x, m, what="misaligned")
+
+
+@pytest.mark.parametrize("lo,hi", [(-1.0, 1.0), (-0.5, 0.25), (0.0, 0.0), (-3.0, 3.0)])
+def test_clamp_bounds(orc, lo, hi):
+    x, m = inputs.epilogue(dev(), shape=(3, 16, 1000))
+    check(orc, x, m, lo, hi, what=f"clamp {lo},{hi}")
+
+
+def test_ties_lowest_index():
+    """Identical channels with identical multipliers tie everywhere."""
+    base = torch.randn(2, 1, 4000, device=dev())
+    x = base.repeat(1, 5, 1).contiguous()
+    m = torch.full((5,), 0.7, device=dev())
+    y, arg = run_epi(x, m)
+    assert bool((arg == 0).all())
+
+
+def test_saturated_channels(orc):
+    """Outliers clamp to exactly hi, so those positions equal m_c exactly."""
+    N, C, S = 2, 4, 4096
+    x = torch.zeros(N, C, S, device=dev())
+    x[:, :, 17] = 1000.0
+    x[:, :, 18:] = torch.randn(N, C, S - 18, device=dev()) * 0.01
+    m = torch.tensor([0.5, 1.5, -2.0, 1.25], device=dev())
+    y, arg = check(orc, x, m, what="saturation")
+    assert bool((y[:, 17] == 1.5).all()) and bool((arg[:, 17] == 1).all())
+
+
+def test_deterministic():
+    x, m = inputs.epilogue(dev(), shape=(6, 16, 14, 30, 30))
+    y1, a1 = run_epi(x, m)
+    y2, a2 = run_epi(x, m)
+    assert torch.equal(y1, y2) and torch.equal(a1, a2)
+
+
+def test_no_argmax_output(orc):
+    x, m = inputs.epilogue(dev(), shape=(3, 16, 14, 30, 30))
+    y, _ = run_epi(x, m, want_arg=False)
+    ref, _, _ = orc.epilogue(x.cpu().numpy().reshape(3, 16, -1), m.cpu().numpy(), EPS)
+    assert_close(y.cpu().numpy(), ref, torch.float32, "no argmax")
+
+
+def test_bounded_wait_timeout(orc, monkeypatch):
+    """The test hook makes one CTA wait on an mbarrier nothing completes: the
+    wait expires after its limit, the error word reports FNORM_ERR_TIMEOUT,
+    the context stays usable and the results are still correct."""
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    x, m = inputs.epilogue(dev(), shape=(2, 16, 14, 30, 30))
+    y, arg = run_epi(x, m)
+    assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
+    assert fn.fnorm_get_last_error() == fn.Status.OK   # read-and-clear
+    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    ref, _, _ = orc.epilogue(x.cpu().numpy().reshape(2, 16, -1), m.cpu().numpy(), EPS)
+    assert_close(y.cpu().numpy(), ref, torch.float32, "after timeout")
+    check(orc, x, m, what="after timeout")

@@ -1,0 +1,192 @@
+"""InstanceNorm on the GPU through the C ABI against the oracle: every kernel
+shape (group, resident, resident cluster, stream), vector and element-wise
+access, all dtype pairs, ragged and degenerate sizes, misaligned pointers,
+in-place use, statistics outputs, determinism and guard bands."""
+import numpy as np
+import pytest
+import torch
+
+import normalization_reduction_gb300 as fn
+from normalization_reduction_gb300 import inputs
+from tests.gpu_util import Guarded, assert_close, code, dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-5
+
+
+def run_in(x: torch.Tensor, out_dtype=None, eps=EPS, out=None, stats=False, NC=None, S=None):
+    out_dtype = out_dtype or x.dtype
+    if S is None:
+        S = x.shape[-1]
+    if NC is None:
+        NC = x.numel() // S if S else 0
+    y = out if out is not None else torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    mean = torch.empty(max(NC, 1), dtype=torch.float32, device=x.device) if stats else None
+    rstd = torch.empty(max(NC, 1), dtype=torch.float32, device=x.device) if stats else None
+    fn.fnorm_instancenorm(x, y, 1, NC, S, code(x.dtype), code(out_dtype), eps, mean, rstd)
+    torch.cuda.synchronize()
+    return y, mean, rstd
+
+
+def oracle_in(orc, x: torch.Tensor, eps=EPS):
+    S = x.shape[-1]
+    ref, mean, var = orc.instancenorm(to_f64(x).reshape(-1, S), eps)
+    return ref.reshape(x.shape), mean, var
+
+
+def make_x(NC, S, dtype, seed, dist="normal"):
+    if dist == "normal":
+        x = inputs.normal((NC, S), seed, "cpu", mean=0.0, std=1.0)
+    elif dist == "shifted":
+        x = inputs.normal((NC, S), seed, "cpu", mean=3.0, std=2.0)
+    else:
+        x = inputs.uniform((NC, S), seed, "cpu")
+    return x.to(dtype).to(dev())
+
+
+def test_small_workload(orc):
+    """x[2,4,16,16] ~ N(0,1) with slice (1,3) = 5.0: parity and exact zeros."""
+    x = inputs.instancenorm_small("cpu")
+    xd = x.to(dev())
+    y = torch.empty_like(xd)
+    fn.fnorm_instancenorm(xd, y, 2, 4, 256, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None)
+    torch.cuda.synchronize()
+    ref, _, _ = orc.instancenorm(x.numpy().reshape(8, 256), EPS)
+    got = y.cpu().numpy().reshape(8, 256)
+    assert_close(got, ref, torch.float32, "small")
+    assert np.all(got[7] == 0.0) and not np.any(np.signbit(got[7]))
+
+
+SIZES = [1, 2, 3, 4, 7, 8, 31, 33, 64, 255, 256, 257, 1000, 1024, 2047, 2048, 4097, 12600,
+         16387, 32768, 65536, 100003, 262144]
+
+
+@pytest.mark.parametrize("S", SIZES)
+@pytest.mark.parametrize("dt", ["f32", "bf16", "bf16>f32", "f32>bf16"])
+def test_sizes_and_dtypes(orc, S, dt):
+    tin = torch.bfloat16 if dt.startswith("bf16") else torch.float32
+    tout = {"f32": torch.float32, "bf16": torch.bfloat16, "bf16>f32": torch.float32,
+            "f32>bf16": torch.bfloat16}[dt]
+    NC = max(3, min(40, 2_000_000 // max(S, 1)))
+    x = make_x(NC, S, tin, 10_000 + S, "shifted" if tin == torch.bfloat16 else "normal")
+    g = Guarded((NC, S), tout)
+    y, mean, rstd = run_in(x, tout, out=g.view, stats=True)
+    g.check()
+    ref, rmean, rvar = oracle_in(orc, x)
+    assert_close(to_f64(y), ref, tout, f"S={S} {dt}")
+    assert_close(mean.cpu().numpy()[:NC], rmean, torch.float32, "mean")
+    assert np.allclose(rstd.cpu().numpy()[:NC], 1.0 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)
+
+
+FORCED = [
+    ("group:8:1", [1, 5, 32]), ("group:8:4", [32, 100, 128]), ("group:32:2", [64, 250]),
+    ("group:32:4", [7, 512]), ("group:32:8", [1024, 999]),
+    ("resident:128:4", [1, 2048, 1500]), ("resident:256:4", [4096, 333]),
+    ("resident:256:8", [8192, 6000]), ("resident:512:8", [16384, 9999]),
+    ("resident:1024:8", [32768, 20000]),
+    ("resident:128:4:3", [5000, 6144, 1]), ("resident:256:8:2", [8193, 16384]),
+    ("resident:512:8:8", [131072, 70000]), ("resident:1024:8:4", [131072, 100001]),
+    ("resident:512:8:16", [262144, 200000]), ("resident:1024:8:16", [524288]),
+    ("stream:1", [1, 77777]), ("stream:2", [12600, 3]), ("stream:8", [262144, 99999]),
+    ("stream:16", [600000]),
+]
+
+
+@pytest.mark.parametrize("path,sizes", FORCED, ids=[p for p, _ in FORCED])
+@pytest.mark.parametrize("scalar", [False, True], ids=["vec", "scalar"])
+def test_forced_paths(orc, monkeypatch, path, sizes, scalar):
+    """Every kernel shape, including empty CTAs in a cluster and 16-CTA clusters."""
+    parts = path.split(":")
+    if parts[0] == "resident" and len(parts) == 4:
+        forced = path
+    elif parts[0] == "resident":
+        forced = path + ":1"
+    else:
+        forced = path
+    monkeypatch.setenv("FNORM_FORCE_PATH", forced)
+    if scalar:
+        monkeypatch.setenv("FNORM_FORCE_SCALAR", "1")
+    for S in sizes:
+        for tin in (torch.float32, torch.bfloat16):
+            W = 4 if tin == torch.float32 else 8
+            slots = -(-S // W)
+            if parts[0] == "group" and int(parts[1]) * int(parts[2]) < slots:
+                continue
+            if parts[0] == "resident":
+                cl = int(forced.split(":")[3])
+                if int(parts[1]) * int(parts[2]) * cl < slots:
+                    continue
+            NC = max(2, min(24, 3_000_000 // S))
+            x = make_x(NC, S, tin, 20_000 + S, "shifted")
+            y, _, _ = run_in(x, tin)
+            ref, _, _ = oracle_in(orc, x)
+            assert_close(to_f64(y), ref, tin, f"{forced} S={S} {tin}")
+
+
+@pytest.mark.parametrize("S", [256, 12600, 262144])
+def test_misaligned_pointers(orc, S):
+    """Base pointers one element off a 16-byte boundary take the element-wise path."""
+    for tin, off in ((torch.float32, 1), (torch.bfloat16, 1), (torch.bfloat16, 3)):
+        NC = 5
+        buf = make_x(NC * S + off, 1, tin, 33_000 + S).reshape(-1)
+        x = buf[off:off + NC * S].view(NC, S)
+        g = Guarded((NC, S), tin, offset_elems=off)
+        y, _, _ = run_in(x, tin, out=g.view)
+        g.check()
+        ref, _, _ = oracle_in(orc, x)
+        assert_close(to_f64(y), ref, tin, f"misaligned S={S}")
+
+
+def test_in_place(orc):
+    x = make_x(20, 4096, torch.float32, 44)
+    ref, _, _ = oracle_in(orc, x)
+    fn.fnorm_instancenorm(x, x, 4, 5, 4096, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None)
+    torch.cuda.synchronize()
+    assert_close(to_f64(x), ref, torch.float32, "in place")
+
+
+def test_constant_slices_exact_zero():
+    """Constant slices of awkward values (not exactly summable) give exact zeros."""
+    for S in (3, 1000, 12600, 262144):
+        for v in (5.0, 0.1, -3.7e5, 1e-30):
+            x = torch.full((3, S), v, dtype=torch.float32, device=dev())
+            y, mean, _ = run_in(x, stats=True)
+            assert bool((y == 0).all()), (S, v)
+            assert bool((mean[:3] == np.float32(v)).all()), (S, v)
+
+
+def test_uniform_input(orc):
+    """The page's own test input, torch.rand ~ U[0,1), at a reduced batch."""
+    x = make_x(64, 512 * 512, torch.float32, 55, "uniform")
+    y, _, _ = run_in(x)
+    ref, _, _ = oracle_in(orc, x)
+    assert_close(to_f64(y), ref, torch.float32, "uniform")
+
+
+def test_deterministic():
+    for S in (256, 12600, 262144, 600000):
+        x = make_x(12, S, torch.float32, 66 + S)
+        y1, m1, _ = run_in(x, stats=True)
+        y2, m2, _ = run_in(x, stats=True)
+        assert torch.equal(y1, y2) and torch.equal(m1, m2), S
+
+
+def test_empty_and_eps_zero():
+    x = torch.empty((0, 16), device=dev())
+    y, _, _ = run_in(x, NC=0, S=16)
+    z = torch.randn(4, 100, device=dev())
+    y, _, _ = run_in(z, eps=0.0)
+    assert bool(torch.isfinite(y).all())
+
+
+def test_mixed_scale_slices(orc):
+    """Slices with very different scales and offsets in one call."""
+    S = 4096
+    base = make_x(8, S, torch.float32, 77)
+    scales = torch.tensor([1e-3, 1.0, 1e3, 1e-2, 50.0, 7.0, 1e4, 0.5], device=dev()).view(8, 1)
+    shifts = torch.tensor([0.0, 100.0, -1e3, 5.0, 1e4, -7.0, 3.0, 1e2], device=dev()).view(8, 1)
+    x = (base * scales + shifts).contiguous()
+    y, _, _ = run_in(x)
+    ref, _, _ = oracle_in(orc, x)
+    assert_close(to_f64(y), ref, torch.float32, "mixed scales")
