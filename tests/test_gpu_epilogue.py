@@ -102,14 +102,16 @@ def test_ties_lowest_index():
 
 
 def test_saturated_channels(orc):
-    """Outliers clamp to exactly hi, so those positions equal m_c exactly."""
+    """Outliers clamp to exactly +-1. Since IN(m x) = sign(m) IN(x), a clamped
+    outlier contributes m_c * sign(m_c) = |m_c| exactly, so the largest |m_c|
+    (channel 2, m = -2) wins there with the value 2.0."""
     N, C, S = 2, 4, 4096
     x = torch.zeros(N, C, S, device=dev())
     x[:, :, 17] = 1000.0
     x[:, :, 18:] = torch.randn(N, C, S - 18, device=dev()) * 0.01
     m = torch.tensor([0.5, 1.5, -2.0, 1.25], device=dev())
     y, arg = check(orc, x, m, what="saturation")
-    assert bool((y[:, 17] == 1.5).all()) and bool((arg[:, 17] == 1).all())
+    assert bool((y[:, 17] == 2.0).all()) and bool((arg[:, 17] == 2).all())
 
 
 def test_deterministic():
