@@ -146,6 +146,39 @@ FNORM_API fnorm_status fnorm_batchnorm_train(const float* x, float* y, const flo
                                    int64_t N, int64_t C, int64_t S, void* workspace,
                                    size_t workspace_bytes, fnorm_stream_t stream);
 
+/*
+ * fnorm_batchnorm_train without a workspace argument, for callers that cannot
+ * allocate device memory: code held to a fixed memory budget reserved up
+ * front, plugins whose host owns the allocator and forbids allocation after
+ * start-up, and steady-state loops where a cudaMalloc (which may synchronise
+ * the device) is not acceptable. The source pages have no counterpart to this
+ * entry point; it exists only for such callers.
+ *
+ * Same arguments, results and errors as fnorm_batchnorm_train, minus
+ * workspace/workspace_bytes. The partial statistics go to a scratch array
+ * that the library itself holds in device memory: 2 MiB (2,097,152 bytes) on
+ * every GPU that loads the library, kept until the process exits. Shapes with
+ * fnorm_batchnorm_workspace_size(N, C, S) above 2 MiB are refused with
+ * FNORM_ERR_UNSUPPORTED before any GPU work.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before any stream capture begins. The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * All calls on a device share the one array, and it keeps whatever the last
+ * call left there; nothing in it needs to start at zero because every call
+ * writes each partial before reading it. Calls whose work overlaps on the
+ * GPU (other streams, other host threads) race on the array: order them on
+ * one stream or synchronise between them.
+ */
+FNORM_API fnorm_status fnorm_batchnorm_train_noalloc(const float* x, float* y, const float* gamma,
+                                                     const float* beta, float scale,
+                                                     float* running_mean, float* running_var,
+                                                     float momentum, float eps, float* save_mean,
+                                                     float* save_rstd, int64_t N, int64_t C,
+                                                     int64_t S, fnorm_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 FNORM_API const char* fnorm_status_string(fnorm_status status);
 

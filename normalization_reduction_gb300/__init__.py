@@ -21,7 +21,7 @@ from enum import IntEnum
 __all__ = [
     "FNORM_F32", "FNORM_BF16", "Status", "FnormError", "LIBRARY", "lib",
     "fnorm_instancenorm", "fnorm_instancenorm_epilogue", "fnorm_batchnorm_workspace_size",
-    "fnorm_batchnorm_train", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
+    "fnorm_batchnorm_train", "fnorm_batchnorm_train_noalloc", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
     "instance_norm", "instance_norm_epilogue", "batch_norm_train",
 ]
 
@@ -60,6 +60,8 @@ _SIGNATURES = {
     "fnorm_batchnorm_workspace_size": ([_i64, _i64, _i64], ctypes.c_size_t),
     "fnorm_batchnorm_train": ([_vp, _vp, _vp, _vp, _f32, _vp, _vp, _f32, _f32, _vp, _vp, _i64,
                                _i64, _i64, _vp, ctypes.c_size_t, _vp], _int),
+    "fnorm_batchnorm_train_noalloc": ([_vp, _vp, _vp, _vp, _f32, _vp, _vp, _f32, _f32, _vp, _vp,
+                                       _i64, _i64, _i64, _vp], _int),
     "fnorm_status_string": ([_int], ctypes.c_char_p),
     "fnorm_get_last_error": ([], _int),
     "fnorm_version": ([], _int),
@@ -132,6 +134,17 @@ def fnorm_batchnorm_train(x, y, gamma, beta, scale, running_mean, running_var, m
                                        _ptr(save_mean), _ptr(save_rstd), N, C, S,
                                        _ptr(workspace), workspace_bytes, _stream(stream)),
            "fnorm_batchnorm_train")
+
+
+def fnorm_batchnorm_train_noalloc(x, y, gamma, beta, scale, running_mean, running_var, momentum,
+                                  eps, save_mean, save_rstd, N, C, S, stream=None) -> None:
+    """fnorm_batchnorm_train for callers that cannot allocate: the library's
+    own 2 MiB device scratch stands in for the workspace (see include/fnorm.h)."""
+    _check(lib().fnorm_batchnorm_train_noalloc(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), scale,
+                                               _ptr(running_mean), _ptr(running_var), momentum,
+                                               eps, _ptr(save_mean), _ptr(save_rstd), N, C, S,
+                                               _stream(stream)),
+           "fnorm_batchnorm_train_noalloc")
 
 
 def fnorm_status_string(status: int) -> str:

@@ -22,7 +22,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(HERE, "libfnorm.so")
 HEADER = os.path.join(ROOT, "include", "fnorm.h")
-SOURCES = ["fnorm_api.cu", "in_f32.cu", "in_bf16.cu", "epi_kernels.cu", "bn_kernels.cu"]
+SOURCES = ["fnorm_api.cu", "in_f32.cu", "in_bf16.cu", "epi_kernels.cu", "bn_kernels.cu",
+           "bn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
