@@ -64,16 +64,19 @@ class Workload:
     def bytes_per_step(self) -> int:
         raise NotImplementedError
 
+    def l2_note(self) -> str:
+        return "input larger than L2, no flush"
+
     def step(self, stream):
         raise NotImplementedError
 
 
 class InstanceNormLarge(Workload):
-    name = "instancenorm2d_fp32_112x64x512x512"
     kernel = "in_resident_kernel"
 
     def __init__(self, dev, shape=inputs.SHAPE_LARGE):
         self.shape = shape
+        self.name = "instancenorm2d_fp32_" + "x".join(str(v) for v in shape)
         self.x = inputs.instancenorm_large(dev, shape)
         self.y = torch.empty_like(self.x)
         self.N, self.C = shape[0], shape[1]
@@ -104,6 +107,9 @@ class Epilogue(Workload):
 
     def bytes_per_step(self):
         return self.N * self.C * self.S * 4 + self.N * self.S * 4 + self.C * 4
+
+    def l2_note(self):
+        return f"{len(self.xs)} rotating input/output copies (>= 4x L2)"
 
     def step(self, stream):
         k = self.i % len(self.xs)
@@ -232,6 +238,19 @@ def max_over_ranks(v: float, ws: int) -> float:
     return float(t.item())
 
 
+def make_workload(args, dev) -> Workload:
+    shape = tuple(int(v) for v in args.shape.split(",")) if args.shape else None
+    if args.workload == "in_large":
+        return InstanceNormLarge(dev, shape or inputs.SHAPE_LARGE)
+    if args.workload == "epilogue":
+        return Epilogue(dev)
+    if args.workload == "batchnorm":
+        return BatchNorm(dev)
+    if args.workload.startswith("sweep:"):
+        return Sweep(dev, int(args.workload.split(":")[1]))
+    raise SystemExit(f"unknown workload {args.workload}")
+
+
 def time_workload(wl: Workload, steps: int, warmup: int, ws: int, sample_clocks=False):
     """Device time per step (ms) with CUDA events on the launching stream."""
     stream = torch.cuda.current_stream()
@@ -330,7 +349,7 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     peak, peak_kind = peak_hbm()
 
-    wl = InstanceNormLarge(dev)
+    wl = make_workload(args, dev)
     total_ms, step_ms, clocks = time_workload(wl, args.steps, args.warmup, ws, sample_clocks=True)
     total_ms = max_over_ranks(total_ms, ws)
     ms = total_ms / args.steps
@@ -342,9 +361,9 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded N(0,1), generated on device)",
-        "config": {"workload": wl.name, "shape": list(wl.shape), "eps": 1e-5,
-                   "bytes_per_step": nbytes, "l2": "input larger than L2 (7.5 GB), no flush",
+        "data": "synthetic (seeded, generated on device)",
+        "config": {"workload": wl.name, "shape": list(getattr(wl, "shape", ())), "eps": 1e-5,
+                   "bytes_per_step": nbytes, "l2": wl.l2_note(),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "pct_of_peak": round(100 * value / ws / peak, 2),
         "pct_of_nominal": round(100 * value / ws / NOMINAL_HBM_GBS, 2),
@@ -355,12 +374,13 @@ def run_ours(args):
         "gpu_launches": wl.launches * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_extra:
+    res["dtype"] = wl.dtype
+    if rank == 0 and not args.no_extra and isinstance(wl, InstanceNormLarge):
         res["e2e"] = e2e_instancenorm(wl, max(2, min(args.steps, 5)))
         res["cpu_baseline"] = cpu_baseline(wl.x, wl.S)
     del wl
     torch.cuda.empty_cache()
-    if not args.no_extra:
+    if not args.no_extra and args.workload == "in_large" and args.shape is None:
         res["per_config"] = other_configs(dev, ws, peak)
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -431,6 +451,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip e2e, cpu baseline and the other workloads")
+    ap.add_argument("--workload", default="in_large",
+                    help="in_large | epilogue | batchnorm | sweep:S (S a power of 4, 256..4^10)")
+    ap.add_argument("--shape", default=None,
+                    help="N,C,H,W for in_large (e.g. a smaller case for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

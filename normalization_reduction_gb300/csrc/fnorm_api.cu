@@ -127,15 +127,15 @@ int in_query(const void* arg) {
 
 int in_capacity(int tin, int tout, const InPlan& plan) {
   char key[128];
-  std::snprintf(key, sizeof key, "in|%d|%d|%d|%d|%d|%d|%d|%d", tin, tout,
-                static_cast<int>(plan.path), plan.vec ? 1 : 0, plan.threads, plan.nv, plan.group,
-                plan.cluster);
+  std::snprintf(key, sizeof key, "in|%d|%d|%d|%d|%d|%d|%d|%d|%d", tin, tout,
+                static_cast<int>(plan.path), plan.vec ? 1 : 0, plan.threads, plan.nv, plan.ns,
+                plan.group, plan.cluster);
   InQuery q{tin, tout, plan};
   return occupancy_cached(key, in_query, &q);
 }
 
 // Parses FNORM_FORCE_PATH (test and tuning hook):
-//   group:G:NV | resident:THREADS:NV:CLUSTER | stream:CLUSTER
+//   group:G:NV | resident:THREADS:NV:CLUSTER | split:THREADS:NR:NS:CLUSTER | stream:CLUSTER
 bool in_forced_plan(InPlan* plan) {
   const char* f = env("FNORM_FORCE_PATH");
   if (!f) return false;
@@ -154,6 +154,15 @@ bool in_forced_plan(InPlan* plan) {
     plan->nv = b;
     plan->cluster = c;
     return true;
+  }
+  int d = 0;
+  if (std::sscanf(f, "split:%d:%d:%d:%d", &a, &b, &c, &d) == 4) {
+    plan->path = InPath::kSplit;
+    plan->threads = a;
+    plan->nv = b;
+    plan->ns = c;
+    plan->cluster = d;
+    return plan->vec;   // the split kernel has no element-wise form
   }
   if (std::sscanf(f, "stream:%d", &a) == 1) {
     plan->path = InPath::kStream;
@@ -176,10 +185,13 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
              !env("FNORM_FORCE_SCALAR");
   const int64_t slots = (S + W - 1) / W;
 
-  if (in_forced_plan(&plan)) {
+  if (env("FNORM_FORCE_PATH")) {
+    if (!in_forced_plan(&plan)) return FNORM_ERR_UNSUPPORTED;
     int64_t cap = 0;
     if (plan.path == InPath::kGroup) cap = int64_t(plan.group) * plan.nv;
     if (plan.path == InPath::kResident) cap = int64_t(plan.threads) * plan.nv * plan.cluster;
+    if (plan.path == InPath::kSplit)
+      cap = int64_t(plan.threads) * (plan.nv + plan.ns) * plan.cluster;
     if (plan.path == InPath::kStream) cap = slots;
     if (cap < slots || plan.cluster < 1 || plan.cluster > kMaxCluster) return FNORM_ERR_UNSUPPORTED;
   } else if (slots <= 256) {
@@ -192,6 +204,23 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
         plan.nv = g[1];
         break;
       }
+    }
+  } else if (plan.vec && slots > 1024 && slots <= int64_t(kMaxCluster) * 8192) {
+    // Split-resident: (threads x (8 register + 8 staged) slots) per CTA, one
+    // CTA per slice up to 8192 slots (128 KiB), clusters of 512-thread CTAs
+    // beyond (two CTAs per SM).
+    plan.path = InPath::kSplit;
+    plan.nv = 8;
+    plan.ns = 8;
+    if (slots <= 2048) {
+      plan.threads = 128;
+      plan.cluster = 1;
+    } else if (slots <= 4096) {
+      plan.threads = 256;
+      plan.cluster = 1;
+    } else {
+      plan.threads = 512;
+      plan.cluster = static_cast<int>((slots + 8191) / 8192);
     }
   } else if (slots <= int64_t(kMaxCluster) * 8192) {
     plan.path = InPath::kResident;
@@ -225,6 +254,12 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
   }
 
   int cap = in_capacity(tin, tout, plan);
+  if (cap <= 0 && plan.path == InPath::kSplit && plan.cluster > 8 && !env("FNORM_FORCE_PATH")) {
+    // 16-CTA clusters not available: twice the chunk per CTA, half the CTAs
+    plan.threads = 1024;
+    plan.cluster = static_cast<int>((slots + 16383) / 16384);
+    cap = in_capacity(tin, tout, plan);
+  }
   if (cap <= 0 && plan.path != InPath::kGroup && plan.cluster > 8 && !env("FNORM_FORCE_PATH")) {
     // 16-CTA clusters not available: stream the slice with a portable cluster.
     plan.path = InPath::kStream;
@@ -243,6 +278,14 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
     const int64_t clusters = NC < cap ? NC : cap;
     plan.grid = static_cast<int>(clusters * plan.cluster);
   }
+  if (env("FNORM_DEBUG_PLAN"))
+    std::fprintf(stderr,
+                 "fnorm_instancenorm plan: path=%d vec=%d threads=%d nv=%d ns=%d group=%d "
+                 "cluster=%d grid=%d capacity=%d NC=%lld S=%lld\n",
+                 static_cast<int>(plan.path), plan.vec ? 1 : 0, plan.threads, plan.nv, plan.ns,
+                 plan.group,
+                 plan.cluster, plan.grid, cap, static_cast<long long>(NC),
+                 static_cast<long long>(S));
   *out = plan;
   return FNORM_OK;
 }
@@ -306,6 +349,11 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   if (cap <= 0) return FNORM_ERR_UNSUPPORTED;
   const int64_t clusters = N < cap ? N : cap;
   plan.grid = static_cast<int>(clusters * plan.cluster);
+  if (env("FNORM_DEBUG_PLAN"))
+    std::fprintf(stderr,
+                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d cpc=%d smem=%zu grid=%d "
+                 "capacity=%d\n",
+                 static_cast<int>(plan.path), plan.cluster, plan.cpc, plan.smem, plan.grid, cap);
   *out = plan;
   return FNORM_OK;
 }

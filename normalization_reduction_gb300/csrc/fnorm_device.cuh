@@ -251,6 +251,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     }
   }
 }
+// 16-byte store into the shared memory of CTA `rank` of the cluster, whose
+// mbarrier (same offset as `local_bar` here) receives the completed bytes.
+__device__ __forceinline__ void st_async_v4(const void* local_dst, const uint64_t* local_bar,
+                                            unsigned rank, const float4& v) {
+  const uint32_t dst = dsmem_map(smem_u32(local_dst), rank);
+  const uint32_t bar = dsmem_map(smem_u32(local_bar), rank);
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(dst),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+
 // Global -> this CTA's shared memory, completion signalled on `bar`.
 __device__ __forceinline__ void tma_bulk_g2s(void* smem_dst, const void* gmem_src, unsigned bytes,
                                              uint64_t* bar) {

@@ -27,13 +27,16 @@ enum class InPath : int {
   kGroup = 0,     // G lanes per slice, slice held in registers (short slices)
   kResident = 1,  // one CTA or one cluster of CTAs per slice, slice held in registers
   kStream = 2,    // one cluster per slice, two reads (statistics, then normalise)
+  kSplit = 3,     // one CTA or cluster per slice, chunk split between shared memory (TMA,
+                  // prefetched) and registers; st.async cluster exchange
 };
 
 struct InPlan {
   InPath path;
   bool vec;      // 16-byte vector access (else element-wise)
   int threads;   // CTA size
-  int nv;        // 16-byte slots per thread (group / resident)
+  int nv;        // 16-byte slots per thread (group / resident), register slots (split)
+  int ns;        // staged (shared-memory) slots per thread (split)
   int group;     // lanes per slice (group path)
   int cluster;   // CTAs per slice (resident / stream); 1 = no cluster
   int grid;      // CTAs to launch (0: the launcher sizes the persistent grid)
@@ -42,6 +45,9 @@ struct InPlan {
 // Launch plans the kernel files provide, listed so the dispatcher can choose
 // among them: resident (threads, nv) and group (group, nv) shapes.
 constexpr int kResidentShapes[][2] = {{128, 4}, {256, 4}, {256, 8}, {512, 8}, {1024, 8}};
+// Split shapes: (threads, register slots, staged slots) per thread.
+constexpr int kSplitShapes[][3] = {{128, 8, 8}, {256, 8, 8}, {512, 8, 8}, {1024, 8, 8},
+                                   {256, 8, 0}, {512, 8, 0}, {1024, 8, 0}};
 constexpr int kGroupShapes[][2] = {{8, 1}, {8, 4}, {32, 2}, {32, 4}, {32, 8}};
 constexpr int kStreamThreads = 512;
 constexpr int kStreamUnroll = 4;

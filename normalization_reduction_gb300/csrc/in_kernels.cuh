@@ -384,6 +384,214 @@ __global__ void __launch_bounds__(THREADS) in_stream_kernel(const InParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Split-resident (vector access only): one CTA or one cluster per slice. A
+// CTA's chunk of the slice is THREADS*(NS + NR) 16-byte slots: the first
+// THREADS*NS slots are staged in shared memory by one TMA bulk copy
+// (cp.async.bulk + mbarrier), the remaining THREADS*NR are held in registers
+// (128-bit loads). Splitting the chunk between the two on-chip stores lets a
+// 512-thread CTA hold 128 KiB while two CTAs share an SM, so one SM keeps two
+// slices' traffic in flight. Per slice:
+//   wait for the staged part -> exact per-thread two-pass over both parts ->
+//   warp/CTA Chan merge -> cluster exchange -> normalise and store the staged
+//   part -> barrier -> bulk-copy the NEXT slice's staged part (prefetch) ->
+//   normalise and store the register part -> load the next register part.
+// Cluster exchange: instead of a cluster-wide barrier per slice, each CTA
+// pushes its partial (n, mean, M2) into slot [rank] of every CTA of the
+// cluster with st.async, which completes bytes on the receiver's mbarrier;
+// each CTA waits only for its own barrier and merges the csize slots in rank
+// order, so all CTAs obtain bit-identical statistics. Two slot sets and two
+// barriers alternate by slice parity; a CTA can reuse a set only after every
+// CTA has consumed it (it needs their next partials first).
+// Dynamic shared memory: THREADS*NS*16 bytes.
+// ---------------------------------------------------------------------------
+constexpr int split_min_blocks(int threads, int nr) {
+  return ((nr >= 8 ? 1024 : 1280) / threads) > 0 ? (nr >= 8 ? 1024 : 1280) / threads : 1;
+}
+
+template <int THREADS>
+__device__ __forceinline__ float2 cluster_exchange(const Stat& cta, float4 (*slots)[kMaxCluster],
+                                                   uint64_t* xbar, float2* fin, unsigned csize,
+                                                   unsigned crank, int it, float eps,
+                                                   unsigned* err, bool& xfailed) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (csize == 1) {
+    if (threadIdx.x == 0) *fin = make_float2(cta.mean, rsqrtf(cta.m2 / cta.n + eps));
+  } else {
+    const int b = it & 1;
+    const unsigned phase = (static_cast<unsigned>(it) >> 1) & 1u;
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(&xbar[b], csize * 16u);
+      const float4 v = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+      for (unsigned r = 0; r < csize; ++r) st_async_v4(&slots[b][crank], &xbar[b], r, v);
+    }
+    if (warp == 0) {
+      if (!xfailed && !mbar_wait_bounded(&xbar[b], phase, err)) xfailed = true;
+      Stat s = stat_empty();
+      if (lane < static_cast<int>(csize)) {
+        const float4 v = slots[b][lane];
+        s = Stat{v.x, v.y, v.z};
+      }
+      s = warp_merge<16>(s);
+      if (lane == 0) *fin = make_float2(s.mean, rsqrtf(s.m2 / s.n + eps));
+    }
+  }
+  __syncthreads();
+  return *fin;
+}
+
+template <class Tin, class Tout, int THREADS, int NR, int NS>
+__global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
+    in_split_kernel(const InParams p) {
+  using E = Elem<Tin>;
+  constexpr int W = E::W;
+  extern __shared__ __align__(128) uint4 stage[];   // [NS][THREADS] slots
+  __shared__ Stat warp_part[THREADS / 32];
+  __shared__ __align__(16) float4 slots[2][kMaxCluster];
+  __shared__ float2 fin;
+  __shared__ __align__(8) uint64_t tma_bar;
+  __shared__ __align__(8) uint64_t xbar[2];
+
+  const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
+  const unsigned cid = cluster_id_x(), ncl = ncluster_x();
+  const int tid = threadIdx.x;
+  const Tin* __restrict__ x = static_cast<const Tin*>(p.x);
+  Tout* __restrict__ y = static_cast<Tout*>(p.y);
+  const int64_t S = p.S;
+  const int64_t nvec = S / W;
+  constexpr int64_t kChunk = static_cast<int64_t>(THREADS) * (NR + NS);
+  const int64_t base = static_cast<int64_t>(crank) * kChunk;          // first vector of the chunk
+  const int64_t cvec = base < nvec ? (nvec - base < kChunk ? nvec - base : kChunk) : 0;
+  const int64_t svec = cvec < int64_t(THREADS) * NS ? cvec : int64_t(THREADS) * NS;
+  const int64_t rvec = cvec - svec;
+  const unsigned sbytes = static_cast<unsigned>(svec * 16);
+  const int ns_valid = (NS > 0 && tid < svec) ? clamp_int((svec - tid + THREADS - 1) / THREADS, 0, NS) : 0;
+  const int nr_valid = (NR > 0 && tid < rvec) ? clamp_int((rvec - tid + THREADS - 1) / THREADS, 0, NR) : 0;
+  const int64_t rbase = base + int64_t(THREADS) * NS + tid;   // vector of register slot 0
+  const int nvalid = (ns_valid + nr_valid) * W;
+
+  if (tid == 0) {
+    mbar_init(&tma_bar, 1);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    fence_mbar_init();
+  }
+  if (csize > 1) cluster_sync();   // peers' barriers exist before anyone signals them
+  else __syncthreads();
+
+  bool failed = false, xfailed = false;
+  unsigned tparity = 0;
+  if (tid == 0 && sbytes > 0 && cid < p.NC) {
+    mbar_arrive_expect_tx(&tma_bar, sbytes);
+    tma_bulk_g2s(stage, reinterpret_cast<const uint4*>(x + cid * S) + base, sbytes, &tma_bar);
+  }
+  uint4 r[NR > 0 ? NR : 1];
+  if (cid < p.NC) {
+    const uint4* xv = reinterpret_cast<const uint4*>(x + cid * S) + rbase;
+#pragma unroll
+    for (int k = 0; k < NR; ++k) r[k] = (k < nr_valid) ? ld_v4(xv + k * THREADS) : make_uint4(0, 0, 0, 0);
+  }
+
+  int it = 0;
+  for (int64_t q = cid; q < p.NC; q += ncl, ++it) {
+    if (sbytes > 0 && !failed) {
+      const bool ok = mbar_wait_bounded(&tma_bar, tparity, p.err);
+      failed = __syncthreads_or(!ok) != 0;
+      if (!failed) tparity ^= 1u;
+    }
+    // exact two-pass over this thread's values, shifted by its first value
+    Stat st = stat_empty();
+    if (nvalid > 0) {
+      const float x0 = E::get(ns_valid > 0 ? stage[tid] : r[0], 0);
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        if (k < ns_valid) {
+          const uint4 v = stage[k * THREADS + tid];
+#pragma unroll
+          for (int j = 0; j < W; ++j) s4[j & 3] += E::get(v, j) - x0;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NR; ++k) {
+        if (k < nr_valid) {
+#pragma unroll
+          for (int j = 0; j < W; ++j) s4[j & 3] += E::get(r[k], j) - x0;
+        }
+      }
+      const float n = static_cast<float>(nvalid);
+      const float mean = x0 + ((s4[0] + s4[1]) + (s4[2] + s4[3])) / n;
+      float q4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        if (k < ns_valid) {
+          const uint4 v = stage[k * THREADS + tid];
+#pragma unroll
+          for (int j = 0; j < W; ++j) {
+            const float d = E::get(v, j) - mean;
+            q4[j & 3] = fmaf(d, d, q4[j & 3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NR; ++k) {
+        if (k < nr_valid) {
+#pragma unroll
+          for (int j = 0; j < W; ++j) {
+            const float d = E::get(r[k], j) - mean;
+            q4[j & 3] = fmaf(d, d, q4[j & 3]);
+          }
+        }
+      }
+      st = Stat{n, mean, (q4[0] + q4[1]) + (q4[2] + q4[3])};
+    }
+    const Stat cta = cta_merge<THREADS>(st, warp_part);
+    const float2 mr = cluster_exchange<THREADS>(cta, slots, xbar, &fin, csize, crank, it, p.eps,
+                                                p.err, xfailed);
+    if (crank == 0 && tid == 0) {
+      if (p.mean_out) p.mean_out[q] = mr.x;
+      if (p.rstd_out) p.rstd_out[q] = mr.y;
+    }
+    Tout* yq = y + q * S;
+    // staged part
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      if (k < ns_valid) {
+        const uint4 v = stage[k * THREADS + tid];
+        float o[W];
+#pragma unroll
+        for (int j = 0; j < W; ++j) o[j] = (E::get(v, j) - mr.x) * mr.y;
+        VecStore<Tout, W>::run(yq + (base + int64_t(k) * THREADS + tid) * W, o);
+      }
+    }
+    const int64_t qn = q + ncl;
+    if (NS > 0) {
+      __syncthreads();   // the stage has been read; refill it with the next slice
+      if (tid == 0 && sbytes > 0 && qn < p.NC && !failed) {
+        mbar_arrive_expect_tx(&tma_bar, sbytes);
+        tma_bulk_g2s(stage, reinterpret_cast<const uint4*>(x + qn * S) + base, sbytes, &tma_bar);
+      }
+    }
+    // register part
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+      if (k < nr_valid) {
+        float o[W];
+#pragma unroll
+        for (int j = 0; j < W; ++j) o[j] = (E::get(r[k], j) - mr.x) * mr.y;
+        VecStore<Tout, W>::run(yq + (rbase + int64_t(k) * THREADS) * W, o);
+      }
+    }
+    if (qn < p.NC) {
+      const uint4* xv = reinterpret_cast<const uint4*>(x + qn * S) + rbase;
+#pragma unroll
+      for (int k = 0; k < NR; ++k) r[k] = (k < nr_valid) ? ld_v4(xv + k * THREADS) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (csize > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
+  if (failed && sbytes > 0) mbar_wait_bounded(&tma_bar, tparity, p.err);
+}
+
+// ---------------------------------------------------------------------------
 // Host side: kernel selection, persistent grid sizing, cluster launch.
 // ---------------------------------------------------------------------------
 template <class K>
@@ -409,7 +617,13 @@ static cudaError_t launch_clustered(K kernel, int grid, int threads, int cluster
 }
 
 template <class K>
-static int max_active_clusters(K kernel, int threads, int cluster) {
+static int max_active_clusters(K kernel, int threads, int cluster, size_t smem) {
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   if (cluster > 8) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
         cudaSuccess) {
@@ -419,7 +633,8 @@ static int max_active_clusters(K kernel, int threads, int cluster) {
   }
   if (cluster <= 1) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+        cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
@@ -428,6 +643,7 @@ static int max_active_clusters(K kernel, int threads, int cluster) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
@@ -465,8 +681,22 @@ static void* pick_kernel(const InPlan& plan) {
         return reinterpret_cast<void*>(
             &in_stream_kernel<Tin, Tout, kStreamThreads, kStreamUnroll, VEC>);
       return nullptr;
+    case InPath::kSplit:
+      if (!VEC) return nullptr;
+#define FNORM_SPLIT(T, R, SM)                                        \
+  if (plan.threads == T && plan.nv == R && plan.ns == SM)            \
+    return reinterpret_cast<void*>(&in_split_kernel<Tin, Tout, T, R, SM>);
+      FNORM_SPLIT(128, 8, 8) FNORM_SPLIT(256, 8, 8) FNORM_SPLIT(512, 8, 8) FNORM_SPLIT(1024, 8, 8)
+      FNORM_SPLIT(256, 8, 0) FNORM_SPLIT(512, 8, 0) FNORM_SPLIT(1024, 8, 0)
+#undef FNORM_SPLIT
+      return nullptr;
   }
   return nullptr;
+}
+
+// Dynamic shared memory of a plan (the pipelined path's stage buffer).
+inline size_t in_plan_smem(const InPlan& plan) {
+  return plan.path == InPath::kSplit ? static_cast<size_t>(plan.threads) * plan.ns * 16 : 0;
 }
 
 template <class Tin, class Tout>
@@ -482,7 +712,7 @@ int in_max_active_clusters_t(const InPlan& plan) {
   if (!k) return 0;
   const int threads = plan.path == InPath::kGroup ? 256 : plan.threads;
   const int cl = plan.path == InPath::kGroup ? 1 : plan.cluster;
-  return max_active_clusters(reinterpret_cast<InKernelFn>(k), threads, cl);
+  return max_active_clusters(reinterpret_cast<InKernelFn>(k), threads, cl, in_plan_smem(plan));
 }
 
 template <class Tin, class Tout>
@@ -496,7 +726,13 @@ cudaError_t in_launch_t(const InParams& p, const InPlan& plan, cudaStream_t stre
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
-  return launch_clustered(fn, plan.grid, threads, cl, 0, stream, p);
+  const size_t smem = in_plan_smem(plan);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_clustered(fn, plan.grid, threads, cl, smem, stream, p);
 }
 
 }  // namespace fnorm

@@ -1,5 +1,5 @@
 """InstanceNorm on the GPU through the C ABI against the oracle: every kernel
-shape (group, resident, resident cluster, stream), vector and element-wise
+shape (group, resident, split-resident with TMA staging, stream), vector and element-wise
 access, all dtype pairs, ragged and degenerate sizes, misaligned pointers,
 in-place use, statistics outputs, determinism and guard bands."""
 import numpy as np
@@ -88,6 +88,12 @@ FORCED = [
     ("resident:128:4:3", [5000, 6144, 1]), ("resident:256:8:2", [8193, 16384]),
     ("resident:512:8:8", [131072, 70000]), ("resident:1024:8:4", [131072, 100001]),
     ("resident:512:8:16", [262144, 200000]), ("resident:1024:8:16", [524288]),
+    ("split:128:8:8:1", [8192, 4000, 16]), ("split:256:8:8:1", [16384, 10000, 64]),
+    ("split:512:8:8:1", [32768, 65536, 20000]), ("split:1024:8:8:1", [65536, 131072, 40000]),
+    ("split:512:8:8:3", [40000, 96000, 8]), ("split:512:8:8:8", [262144, 200000]),
+    ("split:512:8:8:16", [524288, 1048576]), ("split:1024:8:8:8", [524288, 1000000]),
+    ("split:256:8:0:1", [8192, 104]), ("split:512:8:0:4", [65536, 50000]),
+    ("split:1024:8:0:8", [262144]),
     ("stream:1", [1, 77777]), ("stream:2", [12600, 3]), ("stream:8", [262144, 99999]),
     ("stream:16", [600000]),
 ]
@@ -98,7 +104,9 @@ FORCED = [
 def test_forced_paths(orc, monkeypatch, path, sizes, scalar):
     """Every kernel shape, including empty CTAs in a cluster and 16-CTA clusters."""
     parts = path.split(":")
-    if parts[0] == "resident" and len(parts) == 4:
+    if parts[0] == "split" and scalar:
+        pytest.skip("the split kernel has vector access only")
+    if parts[0] in ("resident", "split") and len(parts) >= 4:
         forced = path
     elif parts[0] == "resident":
         forced = path + ":1"
@@ -116,6 +124,11 @@ def test_forced_paths(orc, monkeypatch, path, sizes, scalar):
             if parts[0] == "resident":
                 cl = int(forced.split(":")[3])
                 if int(parts[1]) * int(parts[2]) * cl < slots:
+                    continue
+            if parts[0] == "split":
+                if int(parts[1]) * (int(parts[2]) + int(parts[3])) * int(parts[4]) < slots:
+                    continue
+                if S % W:
                     continue
             NC = max(2, min(24, 3_000_000 // S))
             x = make_x(NC, S, tin, 20_000 + S, "shifted")
