@@ -205,22 +205,34 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
         break;
       }
     }
-  } else if (plan.vec && slots > 1024 && slots <= int64_t(kMaxCluster) * 8192) {
-    // Split-resident: (threads x (8 register + 8 staged) slots) per CTA, one
-    // CTA per slice up to 8192 slots (128 KiB), clusters of 512-thread CTAs
-    // beyond (two CTAs per SM).
+  } else if (plan.vec && slots <= int64_t(kMaxCluster) * 8192) {
+    // Split-resident. Up to 4096 slots (64 KiB of input) a CTA of 64..512
+    // threads holds the slice in registers (8 slots per thread); up to 8192
+    // slots a 512-thread CTA holds 8 slots per thread in registers and 8 in
+    // TMA-staged shared memory (two CTAs per SM); longer slices take clusters
+    // of such CTAs. FNORM_SPLIT_SHAPE=threads:nr:ns overrides the CTA shape.
     plan.path = InPath::kSplit;
     plan.nv = 8;
-    plan.ns = 8;
-    if (slots <= 2048) {
-      plan.threads = 128;
-      plan.cluster = 1;
-    } else if (slots <= 4096) {
-      plan.threads = 256;
-      plan.cluster = 1;
-    } else {
+    plan.ns = 0;
+    plan.cluster = 1;
+    if (slots <= 512) plan.threads = 64;
+    else if (slots <= 1024) plan.threads = 128;
+    else if (slots <= 2048) plan.threads = 256;
+    else if (slots <= 4096) plan.threads = 512;
+    else {
       plan.threads = 512;
+      plan.ns = 8;
       plan.cluster = static_cast<int>((slots + 8191) / 8192);
+    }
+    int t = 0, nr = 0, ns = 0;
+    const char* shape = env("FNORM_SPLIT_SHAPE");
+    if (shape && std::sscanf(shape, "%d:%d:%d", &t, &nr, &ns) == 3) {
+      plan.threads = t;
+      plan.nv = nr;
+      plan.ns = ns;
+      const int64_t per = int64_t(t) * (nr + ns);
+      plan.cluster = static_cast<int>((slots + per - 1) / per);
+      if (plan.cluster > kMaxCluster) return FNORM_ERR_UNSUPPORTED;
     }
   } else if (slots <= int64_t(kMaxCluster) * 8192) {
     plan.path = InPath::kResident;

@@ -47,7 +47,8 @@ struct InPlan {
 constexpr int kResidentShapes[][2] = {{128, 4}, {256, 4}, {256, 8}, {512, 8}, {1024, 8}};
 // Split shapes: (threads, register slots, staged slots) per thread.
 constexpr int kSplitShapes[][3] = {{128, 8, 8}, {256, 8, 8}, {512, 8, 8}, {1024, 8, 8},
-                                   {256, 8, 0}, {512, 8, 0}, {1024, 8, 0}};
+                                   {64, 8, 0},  {128, 8, 0}, {256, 8, 0}, {512, 8, 0},
+                                   {1024, 8, 0}};
 constexpr int kGroupShapes[][2] = {{8, 1}, {8, 4}, {32, 2}, {32, 4}, {32, 8}};
 constexpr int kStreamThreads = 512;
 constexpr int kStreamUnroll = 4;

@@ -687,7 +687,8 @@ static void* pick_kernel(const InPlan& plan) {
   if (plan.threads == T && plan.nv == R && plan.ns == SM)            \
     return reinterpret_cast<void*>(&in_split_kernel<Tin, Tout, T, R, SM>);
       FNORM_SPLIT(128, 8, 8) FNORM_SPLIT(256, 8, 8) FNORM_SPLIT(512, 8, 8) FNORM_SPLIT(1024, 8, 8)
-      FNORM_SPLIT(256, 8, 0) FNORM_SPLIT(512, 8, 0) FNORM_SPLIT(1024, 8, 0)
+      FNORM_SPLIT(64, 8, 0) FNORM_SPLIT(128, 8, 0) FNORM_SPLIT(256, 8, 0) FNORM_SPLIT(512, 8, 0)
+      FNORM_SPLIT(1024, 8, 0)
 #undef FNORM_SPLIT
       return nullptr;
   }
