@@ -41,7 +41,11 @@ L2_BYTES = 126 * 1024 * 1024
 
 # DRAM bytes (read + write) per launch of each workload's dominant kernel from
 # one ncu capture (profiles/*.md); None until measured for the current kernel.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/in_split_kernel__instancenorm_fp32_112x64x512x512.md: 1.073997 GB read +
+    # 1.019953 GB written for 1024 slices, scaled by 7 to the 7168-slice launch
+    "instancenorm2d_fp32_112x64x512x512": 14657650000,
+}
 
 
 def peak_hbm():
@@ -72,7 +76,7 @@ class Workload:
 
 
 class InstanceNormLarge(Workload):
-    kernel = "in_resident_kernel"
+    kernel = "in_split_kernel"
 
     def __init__(self, dev, shape=inputs.SHAPE_LARGE):
         self.shape = shape
@@ -92,7 +96,7 @@ class InstanceNormLarge(Workload):
 
 class Epilogue(Workload):
     name = "epilogue_fp32_128x16x14x30x30"
-    kernel = "epi_resident_kernel"
+    kernel = "epi_range_kernel"
 
     def __init__(self, dev, copies=None):
         x, m = inputs.epilogue(dev)

@@ -102,7 +102,8 @@ FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int
  *   clamp   clamp_lo <= clamp_hi; clamp(t) = min(max(t, lo), hi).
  * y and argmax must not overlap x, m or each other.
  * When a sample's C slices fit on chip in one cluster (C*S*4 bytes up to
- * about 3 MiB) x is read once; otherwise each slice is read twice.
+ * about 3 MiB, C <= 1024, x/y/argmax 16-byte aligned and S a multiple of 4)
+ * x is read once; otherwise each slice is read twice.
  */
 FNORM_API fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
                                          int64_t N, int64_t C, int64_t S, float eps,

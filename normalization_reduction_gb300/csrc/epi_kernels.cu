@@ -6,34 +6,41 @@
 //
 // The page plans two kernels (per-(n,c) statistics, then one thread per output
 // position looping over channels), which reads the convolution output twice.
-// Here one thread-block cluster owns one sample n:
-//  * each CTA pulls the full slices of its cpc channels into shared memory with
-//    TMA bulk copies (cp.async.bulk + mbarrier, bounded waits);
-//  * it forms their statistics from shared memory (exact per-thread two-pass
-//    over 16-value register tiles, Chan merges across tiles, warps and CTAs);
-//  * after a cluster barrier every CTA reads the channel coefficients of all
-//    CTAs and, for its share of the output positions, the C channel values at
-//    each position through distributed shared memory, and writes the maximum
-//    (and optionally its channel index) with 128-bit stores.
-// HBM sees one read of x and one write of y. The statistics are formed on x,
-// and the multiplier is folded in exactly by the affine identity
+// Here one thread-block cluster owns one sample n, and CTA r of the cluster
+// owns a contiguous range of output positions FOR ALL C CHANNELS:
+//  * the CTA stages x[n, c, range] for every c in shared memory with C TMA
+//    bulk copies (cp.async.bulk + mbarrier, bounded waits);
+//  * each warp forms the partial statistics of some channels over the range
+//    (exact two-pass over 16-value register tiles, Chan merges);
+//  * the C partials are pushed with st.async into every CTA of the cluster,
+//    completing on the receiver's mbarrier; every CTA merges the partials of
+//    each channel in rank order (bit-identical results in all CTAs);
+//  * each thread then produces its positions from local shared memory:
+//    the max over c of z_c and, optionally, its channel index.
+// HBM sees one read of x and one write of y, and only C*cluster*16 bytes per
+// CTA cross distributed shared memory. The statistics are formed on x, and the
+// multiplier is folded in exactly by the affine identity
 //   IN(m x) = (x - mean_x) * m / sqrt(m^2 var_x + eps),
 // so z_c = m_c * clamp((x - mean_x) * a_c, lo, hi) with a_c = m_c*rsqrt(m_c^2 var_x + eps).
 //
 // A second kernel covers inputs that do not fit (or are not 16-byte aligned):
-// the same cluster-per-sample structure, reading each slice twice from global
-// memory with element-wise loads.
+// one cluster per sample, CTAs owning whole channels, reading each slice twice
+// from global memory with element-wise loads.
 #include "fnorm_device.cuh"
 #include "fnorm_internal.h"
 #include "in_kernels.cuh"
 
 namespace fnorm {
 
-static __host__ __device__ __forceinline__ size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
+static __host__ __device__ __forceinline__ size_t align128(size_t v) {
+  return (v + 127) & ~size_t(127);
+}
 
-size_t epi_resident_smem(int64_t C, int64_t S, int cpc) {
-  return align16(static_cast<size_t>(cpc) * S * sizeof(float)) + static_cast<size_t>(C) * 16 +
-         static_cast<size_t>(cpc) * 16;
+// Shared memory of the range kernel: staged x [C][per] float4, channel
+// coefficients [C], partial slots [2][C][cluster].
+size_t epi_range_smem(int64_t C, int64_t per, int cluster) {
+  return align128(static_cast<size_t>(C) * per * 16) + static_cast<size_t>(C) * 16 +
+         2 * static_cast<size_t>(C) * cluster * 16;
 }
 
 size_t epi_stream_smem(int64_t C, int cluster) {
@@ -44,147 +51,145 @@ __device__ __forceinline__ float epi_z(float v, const float4& cf, float lo, floa
   return cf.z * fminf(fmaxf((v - cf.x) * cf.y, lo), hi);
 }
 
-// Channel coefficients (mean_x, a_c, m_c) from a CTA-level statistic.
+// Channel coefficients (mean_x, a_c, m_c) from a channel's statistic.
 __device__ __forceinline__ float4 epi_coef(const Stat& s, float mc, float eps) {
   const float var = s.m2 / s.n;
   return make_float4(s.mean, mc * rsqrtf(mc * mc * var + eps), mc, 0.f);
 }
 
+__device__ __forceinline__ void epi_update(float z, int c, float& best, int& arg) {
+  if (z > best) {
+    best = z;
+    arg = c;
+  }
+}
+
 template <int THREADS>
-__global__ void __launch_bounds__(THREADS) epi_resident_kernel(const EpiParams p) {
+__global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ Stat warp_part[THREADS / 32];
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t tma_bar;
+  __shared__ __align__(8) uint64_t xbar[2];
   __shared__ __align__(8) uint64_t dbg_bar;
+  constexpr int NWARP = THREADS / 32;
 
   const int64_t S = p.S;
   const int C = static_cast<int>(p.C);
-  const int cpc = p.cpc;
-  float* xs = reinterpret_cast<float*>(smem_raw);                                   // [cpc][S]
-  float4* coef = reinterpret_cast<float4*>(smem_raw + align16(size_t(cpc) * S * 4));  // [C]
-  float4* loc = coef + C;                                                            // [cpc]
-
+  const int64_t per = p.per;                 // position vectors (of 4) per CTA
   const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
   const unsigned cid = cluster_id_x(), ncl = ncluster_x();
-  const int tid = threadIdx.x;
-  const int c0 = static_cast<int>(crank) * cpc;
-  const int nch = C - c0 < 0 ? 0 : (C - c0 < cpc ? C - c0 : cpc);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint4* xs = reinterpret_cast<uint4*>(smem_raw);                                  // [C][per]
+  float4* coef = reinterpret_cast<float4*>(smem_raw + align128(size_t(C) * per * 16));  // [C]
+  float4* slots = coef + C;                                               // [2][C][csize]
   const int64_t nv4 = S / 4;
+  const int64_t v0 = per * crank;
+  const int64_t vr = v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0;   // vectors owned
+  const unsigned seg_bytes = static_cast<unsigned>(vr * 16);
 
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&tma_bar, 1);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     mbar_init(&dbg_bar, 1);
     fence_mbar_init();
   }
-  __syncthreads();
+  if (csize > 1) cluster_sync();   // peers' barriers exist before anyone signals them
+  else __syncthreads();
   // Test hook: a wait on a barrier nothing completes must expire, record the
   // timeout and let the kernel carry on.
   if (p.debug_timeout && cid == 0 && crank == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
 
-  bool failed = false;
-  unsigned parity = 0;
-  for (int64_t n = cid; n < p.N; n += ncl) {
-    const float* xn = p.x + n * C * S;
-    if (nch > 0 && !failed) {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&bar, static_cast<unsigned>(nch * S * 4));
-        for (int j = 0; j < nch; ++j)
-          tma_bulk_g2s(xs + j * S, xn + (c0 + j) * S, static_cast<unsigned>(S * 4), &bar);
-      }
-      const bool ok = mbar_wait_bounded(&bar, parity, p.err);
-      failed = __syncthreads_or(!ok) != 0;
-      if (!failed) parity ^= 1u;
+  auto issue = [&](int64_t n) {
+    // lanes of warp 0 issue one bulk copy per channel
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(&tma_bar, seg_bytes * static_cast<unsigned>(C));
+      __syncwarp();
+      for (int c = lane; c < C; c += 32)
+        tma_bulk_g2s(xs + int64_t(c) * per, p.x + (n * C + c) * S + v0 * 4, seg_bytes, &tma_bar);
     }
+  };
+  if (seg_bytes > 0 && cid < p.N) issue(cid);
 
-    // Statistics of this CTA's channels.
-    for (int j = 0; j < nch; ++j) {
-      const uint4* v4 = reinterpret_cast<const uint4*>(xs + j * S);
+  bool failed = false, xfailed = false;
+  unsigned tparity = 0;
+  int it = 0;
+  for (int64_t n = cid; n < p.N; n += ncl, ++it) {
+    if (seg_bytes > 0 && !failed) {
+      const bool ok = mbar_wait_bounded(&tma_bar, tparity, p.err);
+      failed = __syncthreads_or(!ok) != 0;
+      if (!failed) tparity ^= 1u;
+    }
+    const int b = it & 1;
+    float4* sl = slots + size_t(b) * C * csize;
+    if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
+    // per-channel partial statistics over this CTA's range, one warp per channel
+    for (int c = warp; c < C; c += NWARP) {
+      const uint4* xc = xs + int64_t(c) * per;
       Stat acc = stat_empty();
-      for (int64_t i = tid; i < nv4; i += THREADS * 4) {
+      for (int64_t i = lane; i < vr; i += 32 * 4) {
         uint4 r[4];
         int nvalid = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const bool v = i + u * THREADS < nv4;
-          r[u] = v ? v4[i + u * THREADS] : make_uint4(0, 0, 0, 0);
+          const bool v = i + u * 32 < vr;
+          r[u] = v ? xc[i + u * 32] : make_uint4(0, 0, 0, 0);
           nvalid += v ? 4 : 0;
         }
         acc = chan_merge(acc, tile_stat<float, 4>(r, nvalid));
       }
-      const Stat cta = cta_merge<THREADS>(acc, warp_part);
-      if (tid == 0) loc[j] = epi_coef(cta, __ldg(p.m + c0 + j), p.eps);
-      __syncthreads();
+      acc = warp_merge<32>(acc);
+      const float4 v = make_float4(__shfl_sync(kFullMask, acc.n, 0), __shfl_sync(kFullMask, acc.mean, 0),
+                                   __shfl_sync(kFullMask, acc.m2, 0), 0.f);
+      // lane r pushes the partial to cluster rank r
+      for (unsigned rr = lane; rr < csize; rr += 32)
+        st_async_v4(&sl[size_t(c) * csize + crank], &xbar[b], rr, v);
     }
-    cluster_sync();
-
-    // Every channel's coefficients, from the CTA that owns it.
-    for (int c = tid; c < C; c += THREADS) {
-      const int owner = c / cpc, j = c - owner * cpc;
-      coef[c] = ld_dsmem_f4(dsmem_map(smem_u32(loc + j), owner));
+    // all partials of every channel: merge in rank order
+    if (!xfailed) {
+      const bool ok = mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(it) >> 1) & 1u, p.err);
+      if (__syncthreads_or(!ok)) xfailed = true;
+    }
+    for (int c = warp; c < C; c += NWARP) {
+      Stat s = stat_empty();
+      if (lane < static_cast<int>(csize)) {
+        const float4 v = sl[size_t(c) * csize + lane];
+        s = Stat{v.x, v.y, v.z};
+      }
+      s = warp_merge<16>(s);
+      if (lane == 0) coef[c] = epi_coef(s, __ldg(p.m + c), p.eps);
     }
     __syncthreads();
 
-    // Output positions [p0, p1) in units of 4.
-    const int64_t per = (nv4 + csize - 1) / csize;
-    const int64_t p0 = per * crank, p1 = (p0 + per < nv4) ? p0 + per : nv4;
-    const uint32_t xs_base = smem_u32(xs);
-    for (int64_t pv = p0 + tid; pv < p1; pv += THREADS) {
+    // outputs of this CTA's positions, from local shared memory
+    for (int64_t v = tid; v < vr; v += THREADS) {
       float best[4];
-      int arg[4];
+      int arg[4] = {0, 0, 0, 0};
       {
-        const float4 v = ld_dsmem_f4(dsmem_map(xs_base + static_cast<uint32_t>(pv * 16), 0));
+        const uint4 u = xs[v];
         const float4 cf = coef[0];
-        best[0] = epi_z(v.x, cf, p.lo, p.hi);
-        best[1] = epi_z(v.y, cf, p.lo, p.hi);
-        best[2] = epi_z(v.z, cf, p.lo, p.hi);
-        best[3] = epi_z(v.w, cf, p.lo, p.hi);
-        arg[0] = arg[1] = arg[2] = arg[3] = 0;
-      }
-      int c = 1;
-      // groups of four channels: issue the four remote loads, then compute
-      for (; c + 4 <= C; c += 4) {
-        float4 v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int cc = c + u, owner = cc / cpc, j = cc - owner * cpc;
-          v[u] = ld_dsmem_f4(
-              dsmem_map(xs_base + static_cast<uint32_t>((j * S + pv * 4) * 4), owner));
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 cf = coef[c + u];
-          const float z0 = epi_z(v[u].x, cf, p.lo, p.hi), z1 = epi_z(v[u].y, cf, p.lo, p.hi);
-          const float z2 = epi_z(v[u].z, cf, p.lo, p.hi), z3 = epi_z(v[u].w, cf, p.lo, p.hi);
-          if (z0 > best[0]) { best[0] = z0; arg[0] = c + u; }
-          if (z1 > best[1]) { best[1] = z1; arg[1] = c + u; }
-          if (z2 > best[2]) { best[2] = z2; arg[2] = c + u; }
-          if (z3 > best[3]) { best[3] = z3; arg[3] = c + u; }
-        }
+        for (int j = 0; j < 4; ++j) best[j] = epi_z(Elem<float>::get(u, j), cf, p.lo, p.hi);
       }
-      for (; c < C; ++c) {
-        const int owner = c / cpc, j = c - owner * cpc;
-        const float4 v =
-            ld_dsmem_f4(dsmem_map(xs_base + static_cast<uint32_t>((j * S + pv * 4) * 4), owner));
+      for (int c = 1; c < C; ++c) {
+        const uint4 u = xs[int64_t(c) * per + v];
         const float4 cf = coef[c];
-        const float z0 = epi_z(v.x, cf, p.lo, p.hi), z1 = epi_z(v.y, cf, p.lo, p.hi);
-        const float z2 = epi_z(v.z, cf, p.lo, p.hi), z3 = epi_z(v.w, cf, p.lo, p.hi);
-        if (z0 > best[0]) { best[0] = z0; arg[0] = c; }
-        if (z1 > best[1]) { best[1] = z1; arg[1] = c; }
-        if (z2 > best[2]) { best[2] = z2; arg[2] = c; }
-        if (z3 > best[3]) { best[3] = z3; arg[3] = c; }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) epi_update(epi_z(Elem<float>::get(u, j), cf, p.lo, p.hi), c, best[j], arg[j]);
       }
-      float* yo = p.y + n * S + pv * 4;
-      *reinterpret_cast<float4*>(yo) = make_float4(best[0], best[1], best[2], best[3]);
+      const int64_t pos = (v0 + v) * 4;
+      *reinterpret_cast<float4*>(p.y + n * S + pos) = make_float4(best[0], best[1], best[2], best[3]);
       if (p.argmax) {
-        longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pv * 4);
+        longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pos);
         ao[0] = make_longlong2(arg[0], arg[1]);
         ao[1] = make_longlong2(arg[2], arg[3]);
       }
     }
-    // No CTA may overwrite (or release) shared memory another CTA still reads.
-    cluster_sync();
+    __syncthreads();   // staged data and coefficients consumed
+    const int64_t nn = n + ncl;
+    if (seg_bytes > 0 && nn < p.N && !failed) issue(nn);
   }
-  if (failed && nch > 0) mbar_wait_bounded(&bar, parity, p.err);   // let copies in flight land
+  if (csize > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
+  if (failed && seg_bytes > 0) mbar_wait_bounded(&tma_bar, tparity, p.err);
 }
 
 // Fallback: cluster per sample, CTA rank r owns channels r, r+csize, ...;
@@ -253,8 +258,8 @@ using EpiKernelFn = void (*)(EpiParams);
 
 static EpiKernelFn epi_kernel(const EpiPlan& plan) {
   if (plan.threads != kEpiThreads) return nullptr;
-  return plan.path == EpiPath::kResident ? &epi_resident_kernel<kEpiThreads>
-                                         : &epi_stream_kernel<kEpiThreads>;
+  return plan.path == EpiPath::kRange ? &epi_range_kernel<kEpiThreads>
+                                      : &epi_stream_kernel<kEpiThreads>;
 }
 
 static cudaError_t epi_prepare(EpiKernelFn fn, const EpiPlan& plan) {

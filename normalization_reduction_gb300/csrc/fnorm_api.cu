@@ -316,8 +316,13 @@ int epi_capacity(const EpiPlan& plan) {
   return occupancy_cached(key, epi_query, &q);
 }
 
-constexpr size_t kEpiTargetBytes = 110 * 1024;   // per-CTA share of a sample, 2 CTAs per SM
+constexpr size_t kEpiTargetBytes = 110 * 1024;   // staged bytes per CTA: two CTAs per SM
 
+// Range plan: cluster of CTAs per sample, each CTA staging a range of
+// positions of all C channels. Preferred cluster sizes in order; the first
+// whose per-CTA staging fits kEpiTargetBytes wins, else the first that fits
+// shared memory at all. FNORM_EPI_CLUSTER forces a size, FNORM_EPI_STREAM the
+// two-read kernel.
 fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax, int64_t N,
                            int64_t C, int64_t S, EpiPlan* out) {
   const DeviceInfo& di = device_info();
@@ -327,33 +332,31 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   EpiPlan plan{};
   plan.threads = kEpiThreads;
   bool have = false;
-  if (vec) {
-    const int cands[] = {1, 2, 4, 8, 16};
-    int chosen = 0;
-    for (int pass = 0; pass < 2 && !chosen; ++pass) {
+  if (vec && C <= 1024) {
+    const int cands[] = {8, 16, 4, 2, 1};
+    const int64_t nv4 = S / 4;
+    for (int pass = 0; pass < 2 && !have; ++pass) {
       for (int cl : cands) {
         if (force_cl && cl != std::atoi(force_cl)) continue;
-        const int64_t cpc = (C + cl - 1) / cl;
-        const size_t smem = epi_resident_smem(C, S, static_cast<int>(cpc));
-        const size_t bytes = static_cast<size_t>(cpc) * S * 4;
-        if (smem > static_cast<size_t>(di.max_smem_optin) || bytes >= (size_t(1) << 20)) continue;
-        if (pass == 0 && !force_cl && bytes > kEpiTargetBytes) continue;
-        EpiPlan cand{EpiPath::kResident, kEpiThreads, static_cast<int>((C + cpc - 1) / cpc),
-                     static_cast<int>(cpc), smem, 0};
-        if (cand.cluster < 1) cand.cluster = 1;
+        const int64_t per = (nv4 + cl - 1) / cl;
+        const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
+        const size_t smem = epi_range_smem(C, per, cl_eff);
+        const size_t staged = static_cast<size_t>(C) * per * 16;
+        if (smem > static_cast<size_t>(di.max_smem_optin) || staged >= (size_t(1) << 20)) continue;
+        if (pass == 0 && !force_cl && staged > kEpiTargetBytes) continue;
+        EpiPlan cand{EpiPath::kRange, kEpiThreads, cl_eff, per, smem, 0};
         if (epi_capacity(cand) > 0) {
           plan = cand;
-          chosen = cl;
+          have = true;
           break;
         }
       }
     }
-    have = chosen != 0;
   }
   if (!have) {
     plan.path = EpiPath::kStream;
     plan.cluster = kEpiStreamCluster;
-    plan.cpc = 0;
+    plan.per = 0;
     plan.smem = epi_stream_smem(C, plan.cluster);
     if (plan.smem > static_cast<size_t>(di.max_smem_optin)) return FNORM_ERR_UNSUPPORTED;
   }
@@ -363,9 +366,10 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   plan.grid = static_cast<int>(clusters * plan.cluster);
   if (env("FNORM_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d cpc=%d smem=%zu grid=%d "
+                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d per=%lld smem=%zu grid=%d "
                  "capacity=%d\n",
-                 static_cast<int>(plan.path), plan.cluster, plan.cpc, plan.smem, plan.grid, cap);
+                 static_cast<int>(plan.path), plan.cluster, static_cast<long long>(plan.per),
+                 plan.smem, plan.grid, cap);
   *out = plan;
   return FNORM_OK;
 }
@@ -501,8 +505,8 @@ fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* 
   if (st != FNORM_OK) return st;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
-  EpiParams p{x, m, y, argmax, N, C, S, eps, clamp_lo, clamp_hi, plan.cpc,
-              (env("FNORM_DEBUG_FORCE_TIMEOUT") && plan.path == EpiPath::kResident) ? 1 : 0, err};
+  EpiParams p{x, m, y, argmax, N, C, S, eps, clamp_lo, clamp_hi, plan.per,
+              (env("FNORM_DEBUG_FORCE_TIMEOUT") && plan.path == EpiPath::kRange) ? 1 : 0, err};
   return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -75,18 +75,18 @@ struct EpiParams {
   float eps;
   float lo;
   float hi;
-  int cpc;             // channels held per CTA (resident path)
+  int64_t per;         // position vectors (of 4) per CTA (range path)
   int debug_timeout;   // test hook: wait on an mbarrier nobody completes
   unsigned* err;
 };
 
-enum class EpiPath : int { kResident = 0, kStream = 1 };
+enum class EpiPath : int { kRange = 0, kStream = 1 };
 
 struct EpiPlan {
   EpiPath path;
   int threads;
   int cluster;
-  int cpc;
+  int64_t per;
   size_t smem;   // dynamic shared memory bytes
   int grid;      // CTAs (multiple of cluster)
 };
@@ -97,7 +97,7 @@ constexpr int kEpiMaxChannels = 8192;
 
 cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t stream);
 int epi_max_active_clusters(const EpiPlan& plan);
-size_t epi_resident_smem(int64_t C, int64_t S, int cpc);
+size_t epi_range_smem(int64_t C, int64_t per, int cluster);
 size_t epi_stream_smem(int64_t C, int cluster);
 
 // ---------------------------------------------------------------- BatchNorm
