@@ -66,9 +66,11 @@ __global__ void __launch_bounds__(THREADS) bn_stats_kernel(const BnParams p) {
   const int64_t n = b / p.chunks, k = b - n * p.chunks;
   const float* xr = p.x + (n * p.C + c) * p.S;
   const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
+  pdl_wait();
   const Stat cta = cta_merge<THREADS>(bn_range_stat<THREADS, U, VEC>(xr, lo, hi), warp_part);
   if (threadIdx.x == 0)
     p.partials[c * (p.N * p.chunks) + b] = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+  pdl_trigger();
 }
 
 template <int THREADS>
@@ -77,6 +79,7 @@ __global__ void __launch_bounds__(THREADS) bn_finalize_kernel(const BnParams p) 
   const int64_t c = blockIdx.x;
   const int64_t P = p.N * p.chunks;
   const float4* part = p.partials + c * P;
+  pdl_wait();
   Stat acc = stat_empty();
   for (int64_t i = threadIdx.x; i < P; i += THREADS) {
     const float4 v = part[i];
@@ -100,6 +103,7 @@ __global__ void __launch_bounds__(THREADS) bn_finalize_kernel(const BnParams p) 
       p.running_var[c] = static_cast<float>((1.0 - mom) * p.running_var[c] + mom * unbiased);
     }
   }
+  pdl_trigger();
 }
 
 template <int THREADS, int U, bool VEC>
@@ -114,6 +118,7 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
   const float* xr = p.x + off;
   float* yr = p.y + off;
   const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
+  pdl_wait();
   const float4 cf = p.coef[c];
   const int tid = threadIdx.x;
   constexpr int64_t TILE = static_cast<int64_t>(THREADS) * U * 4;
@@ -144,17 +149,30 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
   }
 }
 
+// Stream-ordered launch with programmatic dependent launch allowed.
+static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream_t stream,
+                                 const BnParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kBnThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <bool VEC>
 static cudaError_t bn_launch_t(const BnParams& p, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
-  bn_stats_kernel<kBnThreads, kBnUnroll, VEC><<<grid, kBnThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = bn_launch_one(&bn_stats_kernel<kBnThreads, kBnUnroll, VEC>, grid, stream, p);
   if (e != cudaSuccess) return e;
-  bn_finalize_kernel<kBnThreads><<<static_cast<unsigned>(p.C), kBnThreads, 0, stream>>>(p);
-  e = cudaGetLastError();
+  e = bn_launch_one(&bn_finalize_kernel<kBnThreads>, dim3(static_cast<unsigned>(p.C), 1, 1),
+                    stream, p);
   if (e != cudaSuccess) return e;
-  bn_apply_kernel<kBnThreads, kBnUnroll, VEC><<<grid, kBnThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, VEC>, grid, stream, p);
 }
 
 cudaError_t bn_launch(const BnParams& p, cudaStream_t stream) {

@@ -36,11 +36,15 @@ static __host__ __device__ __forceinline__ size_t align128(size_t v) {
   return (v + 127) & ~size_t(127);
 }
 
-// Shared memory of the range kernel: staged x [C][per] float4, channel
-// coefficients [C], partial slots [2][C][cluster].
+// Shared memory of the range kernel: two staging buffers of x [C][per]
+// float4, channel coefficients [C], partial slots [2][C][cluster].
 size_t epi_range_smem(int64_t C, int64_t per, int cluster) {
-  return align128(static_cast<size_t>(C) * per * 16) + static_cast<size_t>(C) * 16 +
+  return 2 * align128(static_cast<size_t>(C) * per * 16) + static_cast<size_t>(C) * 16 +
          2 * static_cast<size_t>(C) * cluster * 16;
+}
+
+size_t epi_range_l2_smem(int64_t C, int cluster) {
+  return static_cast<size_t>(C) * 16 + 2 * static_cast<size_t>(C) * cluster * 16;
 }
 
 size_t epi_stream_smem(int64_t C, int cluster) {
@@ -64,10 +68,29 @@ __device__ __forceinline__ void epi_update(float z, int c, float& best, int& arg
   }
 }
 
-template <int THREADS>
+// Per-channel output coefficients: z_c = clamp(x*A + B, lo_c, hi_c) with
+// A = m_c*a_c, B = -mean_x*A, and (lo_c, hi_c) = m_c*(lo, hi) ordered for the
+// sign of m_c -- the same value as m_c*clamp((x - mean_x)*a_c, lo, hi) since
+// multiplying by m_c is monotone (order-reversing for m_c < 0).
+__device__ __forceinline__ float4 epi_out_coef(const Stat& s, float mc, float eps, float lo,
+                                               float hi) {
+  const float var = s.m2 / s.n;
+  const float A = mc * (mc * rsqrtf(mc * mc * var + eps));
+  const float l = mc * lo, h = mc * hi;
+  return make_float4(A, -s.mean * A, fminf(l, h), fmaxf(l, h));
+}
+
+__device__ __forceinline__ float epi_zc(float v, const float4& k) {
+  return fminf(fmaxf(fmaf(v, k.x, k.y), k.z), k.w);
+}
+
+// Range kernel: cluster per sample, CTA r staging positions [r*per, ...) of all
+// C channels, double-buffered: while sample n is reduced and written, the
+// CTA's staging of sample n + 2*clusters is already in flight.
+template <int THREADS, bool WANT_ARG>
 __global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t tma_bar;
+  __shared__ __align__(8) uint64_t sbar[2];
   __shared__ __align__(8) uint64_t xbar[2];
   __shared__ __align__(8) uint64_t dbg_bar;
   constexpr int NWARP = THREADS / 32;
@@ -78,16 +101,18 @@ __global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
   const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
   const unsigned cid = cluster_id_x(), ncl = ncluster_x();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint4* xs = reinterpret_cast<uint4*>(smem_raw);                                  // [C][per]
-  float4* coef = reinterpret_cast<float4*>(smem_raw + align128(size_t(C) * per * 16));  // [C]
-  float4* slots = coef + C;                                               // [2][C][csize]
+  const size_t stage_bytes = align128(size_t(C) * per * 16);
+  uint4* stage0 = reinterpret_cast<uint4*>(smem_raw);                       // [2][C][per]
+  float4* coef = reinterpret_cast<float4*>(smem_raw + 2 * stage_bytes);     // [C]
+  float4* slots = coef + C;                                                  // [2][C][csize]
   const int64_t nv4 = S / 4;
   const int64_t v0 = per * crank;
   const int64_t vr = v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0;   // vectors owned
   const unsigned seg_bytes = static_cast<unsigned>(vr * 16);
 
   if (tid == 0) {
-    mbar_init(&tma_bar, 1);
+    mbar_init(&sbar[0], 1);
+    mbar_init(&sbar[1], 1);
     mbar_init(&xbar[0], 1);
     mbar_init(&xbar[1], 1);
     mbar_init(&dbg_bar, 1);
@@ -95,31 +120,31 @@ __global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
   }
   if (csize > 1) cluster_sync();   // peers' barriers exist before anyone signals them
   else __syncthreads();
-  // Test hook: a wait on a barrier nothing completes must expire, record the
-  // timeout and let the kernel carry on.
-  if (p.debug_timeout && cid == 0 && crank == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
+  pdl_wait();
 
-  auto issue = [&](int64_t n) {
-    // lanes of warp 0 issue one bulk copy per channel
-    if (warp == 0) {
-      if (lane == 0) mbar_arrive_expect_tx(&tma_bar, seg_bytes * static_cast<unsigned>(C));
-      __syncwarp();
-      for (int c = lane; c < C; c += 32)
-        tma_bulk_g2s(xs + int64_t(c) * per, p.x + (n * C + c) * S + v0 * 4, seg_bytes, &tma_bar);
-    }
+  auto stage_of = [&](int b) { return reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(stage0) + b * stage_bytes); };
+  // One thread stages sample n into buffer b: C bulk copies, one barrier.
+  auto issue = [&](int64_t n, int b) {
+    mbar_arrive_expect_tx(&sbar[b], seg_bytes * static_cast<unsigned>(C));
+    uint4* st = stage_of(b);
+    for (int c = 0; c < C; ++c)
+      tma_bulk_g2s(st + int64_t(c) * per, p.x + (n * C + c) * S + v0 * 4, seg_bytes, &sbar[b]);
   };
-  if (seg_bytes > 0 && cid < p.N) issue(cid);
+  if (seg_bytes > 0 && tid == 0) {
+    if (cid < p.N) issue(cid, 0);
+    if (cid + ncl < p.N) issue(cid + ncl, 1);
+  }
 
   bool failed = false, xfailed = false;
-  unsigned tparity = 0;
   int it = 0;
   for (int64_t n = cid; n < p.N; n += ncl, ++it) {
-    if (seg_bytes > 0 && !failed) {
-      const bool ok = mbar_wait_bounded(&tma_bar, tparity, p.err);
-      failed = __syncthreads_or(!ok) != 0;
-      if (!failed) tparity ^= 1u;
-    }
     const int b = it & 1;
+    const unsigned use_parity = (static_cast<unsigned>(it) >> 1) & 1u;   // k-th use of buffer b
+    const uint4* xs = stage_of(b);
+    if (seg_bytes > 0 && !failed) {
+      const bool ok = mbar_wait_bounded(&sbar[b], use_parity, p.err);
+      failed = __syncthreads_or(!ok) != 0;
+    }
     float4* sl = slots + size_t(b) * C * csize;
     if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
     // per-channel partial statistics over this CTA's range, one warp per channel
@@ -146,6 +171,160 @@ __global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
     }
     // all partials of every channel: merge in rank order
     if (!xfailed) {
+      const bool ok = mbar_wait_bounded(&xbar[b], use_parity, p.err);
+      if (__syncthreads_or(!ok)) xfailed = true;
+    }
+    for (int c = warp; c < C; c += NWARP) {
+      Stat s = stat_empty();
+      if (lane < static_cast<int>(csize)) {
+        const float4 v = sl[size_t(c) * csize + lane];
+        s = Stat{v.x, v.y, v.z};
+      }
+      s = warp_merge<16>(s);
+      if (lane == 0) coef[c] = epi_out_coef(s, __ldg(p.m + c), p.eps, p.lo, p.hi);
+    }
+    __syncthreads();
+
+    // outputs of this CTA's positions, from the staged data
+    for (int64_t v = tid; v < vr; v += THREADS) {
+      float best[4];
+      int arg[4] = {0, 0, 0, 0};
+      {
+        const uint4 u = xs[v];
+        const float4 k = coef[0];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) best[j] = epi_zc(Elem<float>::get(u, j), k);
+      }
+      for (int c = 1; c < C; ++c) {
+        const uint4 u = xs[int64_t(c) * per + v];
+        const float4 k = coef[c];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float z = epi_zc(Elem<float>::get(u, j), k);
+          if (WANT_ARG) {
+            if (z > best[j]) {
+              best[j] = z;
+              arg[j] = c;
+            }
+          } else {
+            best[j] = fmaxf(best[j], z);
+          }
+        }
+      }
+      const int64_t pos = (v0 + v) * 4;
+      *reinterpret_cast<float4*>(p.y + n * S + pos) = make_float4(best[0], best[1], best[2], best[3]);
+      if (WANT_ARG) {
+        longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pos);
+        ao[0] = make_longlong2(arg[0], arg[1]);
+        ao[1] = make_longlong2(arg[2], arg[3]);
+      }
+    }
+    __syncthreads();   // buffer b and the coefficients consumed
+    const int64_t nn = n + 2 * int64_t(ncl);
+    if (seg_bytes > 0 && tid == 0 && nn < p.N && !failed) issue(nn, b);
+  }
+  pdl_trigger();
+  if (csize > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
+  if (failed && seg_bytes > 0) {   // let copies that may still be in flight land
+    mbar_wait_bounded(&sbar[0], 0, p.err);
+    mbar_wait_bounded(&sbar[1], 0, p.err);
+  }
+  // Test hook, after the last cluster barrier so no peer waits on this CTA:
+  // a wait on a barrier nothing completes must expire, record the timeout in
+  // the error word and return.
+  if (p.debug_timeout && cid == 0 && crank == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
+}
+
+// Range kernel, L2 form: the same decomposition (cluster per sample, CTA r
+// owning a range of positions of all channels, st.async exchange of the
+// per-channel partials) without staging. The statistics pass streams x from
+// HBM with 128-bit loads, 8 per lane in flight, leaving it in L2; the output
+// pass reads the CTA's range again from L2 (4 channels' loads in flight per
+// thread). For the page's shape a sample is 806 KB and the whole input
+// 103 MB, below the 126 MB L2; with 256-thread CTAs in 4-CTA clusters every
+// sample's cluster is resident at once, so HBM still sees one read of x.
+template <bool WANT_ARG>
+__device__ __forceinline__ void epi_take(const uint4& u, const float4& k, int c, float (&best)[4],
+                                         int (&arg)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float z = epi_zc(Elem<float>::get(u, j), k);
+    if (WANT_ARG) {
+      if (z > best[j]) {
+        best[j] = z;
+        arg[j] = c;
+      }
+    } else {
+      best[j] = fmaxf(best[j], z);
+    }
+  }
+}
+
+template <int THREADS, bool WANT_ARG>
+__global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParams p) {
+  extern __shared__ __align__(16) float4 dyn[];
+  __shared__ __align__(8) uint64_t xbar[2];
+  __shared__ __align__(8) uint64_t dbg_bar;
+  constexpr int NWARP = THREADS / 32;
+  constexpr int U = 8;    // 16-byte loads per lane per statistics tile
+  constexpr int G = 4;    // channels loaded together in the output pass
+  const int64_t S = p.S;
+  const int C = static_cast<int>(p.C);
+  const int64_t per = p.per;
+  const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
+  const unsigned cid = cluster_id_x(), ncl = ncluster_x();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float4* coef = dyn;          // [C]
+  float4* slots = dyn + C;     // [2][C][csize]
+  const int64_t nv4 = S / 4;
+  const int64_t v0 = per * crank;
+  const int vr = static_cast<int>(v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0);
+
+  if (tid == 0) {
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    mbar_init(&dbg_bar, 1);
+    fence_mbar_init();
+  }
+  if (csize > 1) cluster_sync();
+  else __syncthreads();
+  pdl_wait();
+
+  bool xfailed = false;
+  int it = 0;
+  for (int64_t n = cid; n < p.N; n += ncl, ++it) {
+    const int b = it & 1;
+    float4* sl = slots + size_t(b) * C * csize;
+    if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
+    const uint4* xn = reinterpret_cast<const uint4*>(p.x + n * C * S) + v0;
+    for (int c = warp; c < C; c += NWARP) {
+      const uint4* xc = xn + int64_t(c) * nv4 + lane;
+      Stat acc = stat_empty();
+      int t = 0;
+      for (; t + 32 * U <= vr; t += 32 * U) {   // full tiles
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = ld_v4(xc + t + u * 32);
+        acc = chan_merge(acc, tile_stat_full<float, U>(r));
+      }
+      if (t < vr) {                              // ragged tail
+        uint4 r[U];
+        int nvalid = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const bool v = t + u * 32 + lane < vr;
+          r[u] = v ? ld_v4(xc + t + u * 32) : make_uint4(0, 0, 0, 0);
+          nvalid += v ? 4 : 0;
+        }
+        acc = chan_merge(acc, tile_stat<float, U>(r, nvalid));
+      }
+      acc = warp_merge<32>(acc);
+      const float4 v = make_float4(__shfl_sync(kFullMask, acc.n, 0), __shfl_sync(kFullMask, acc.mean, 0),
+                                   __shfl_sync(kFullMask, acc.m2, 0), 0.f);
+      for (unsigned rr = lane; rr < csize; rr += 32)
+        st_async_v4(&sl[size_t(c) * csize + crank], &xbar[b], rr, v);
+    }
+    if (!xfailed) {
       const bool ok = mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(it) >> 1) & 1u, p.err);
       if (__syncthreads_or(!ok)) xfailed = true;
     }
@@ -156,40 +335,44 @@ __global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
         s = Stat{v.x, v.y, v.z};
       }
       s = warp_merge<16>(s);
-      if (lane == 0) coef[c] = epi_coef(s, __ldg(p.m + c), p.eps);
+      if (lane == 0) coef[c] = epi_out_coef(s, __ldg(p.m + c), p.eps, p.lo, p.hi);
     }
     __syncthreads();
-
-    // outputs of this CTA's positions, from local shared memory
-    for (int64_t v = tid; v < vr; v += THREADS) {
+    for (int v = tid; v < vr; v += THREADS) {
+      const uint4* xv = xn + v;
       float best[4];
       int arg[4] = {0, 0, 0, 0};
       {
-        const uint4 u = xs[v];
-        const float4 cf = coef[0];
+        const uint4 u = __ldcs(xv);
+        const float4 k = coef[0];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) best[j] = epi_z(Elem<float>::get(u, j), cf, p.lo, p.hi);
+        for (int j = 0; j < 4; ++j) best[j] = epi_zc(Elem<float>::get(u, j), k);
       }
-      for (int c = 1; c < C; ++c) {
-        const uint4 u = xs[int64_t(c) * per + v];
-        const float4 cf = coef[c];
+      int c = 1;
+      for (; c + G <= C; c += G) {
+        uint4 u[G];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) epi_update(epi_z(Elem<float>::get(u, j), cf, p.lo, p.hi), c, best[j], arg[j]);
+        for (int g = 0; g < G; ++g) u[g] = __ldcs(xv + int64_t(c + g) * nv4);
+#pragma unroll
+        for (int g = 0; g < G; ++g) epi_take<WANT_ARG>(u[g], coef[c + g], c + g, best, arg);
       }
+      for (; c < C; ++c) epi_take<WANT_ARG>(__ldcs(xv + int64_t(c) * nv4), coef[c], c, best, arg);
       const int64_t pos = (v0 + v) * 4;
-      *reinterpret_cast<float4*>(p.y + n * S + pos) = make_float4(best[0], best[1], best[2], best[3]);
-      if (p.argmax) {
+      __stcs(reinterpret_cast<float4*>(p.y + n * S + pos), make_float4(best[0], best[1], best[2], best[3]));
+      if (WANT_ARG) {
         longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pos);
-        ao[0] = make_longlong2(arg[0], arg[1]);
-        ao[1] = make_longlong2(arg[2], arg[3]);
+        __stcs(ao, make_longlong2(arg[0], arg[1]));
+        __stcs(ao + 1, make_longlong2(arg[2], arg[3]));
       }
     }
-    __syncthreads();   // staged data and coefficients consumed
-    const int64_t nn = n + ncl;
-    if (seg_bytes > 0 && nn < p.N && !failed) issue(nn);
+    __syncthreads();   // coefficients consumed before the next sample rewrites them
   }
-  if (csize > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
-  if (failed && seg_bytes > 0) mbar_wait_bounded(&tma_bar, tparity, p.err);
+  pdl_trigger();
+  if (csize > 1) cluster_sync();
+  // Test hook, after the last cluster barrier so no peer waits on this CTA:
+  // a wait on a barrier nothing completes must expire, record the timeout in
+  // the error word and return.
+  if (p.debug_timeout && cid == 0 && crank == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
 // Fallback: cluster per sample, CTA rank r owns channels r, r+csize, ...;
@@ -208,6 +391,7 @@ __global__ void __launch_bounds__(THREADS) epi_stream_kernel(const EpiParams p) 
   float4* loc = dyn4 + C;    // [ceil(C / csize)]
   constexpr int TILE = THREADS * 16;   // elements per tile: 16 per thread
 
+  pdl_wait();
   for (int64_t n = cid; n < p.N; n += ncl) {
     for (int c = static_cast<int>(crank), jl = 0; c < C; c += csize, ++jl) {
       const float* xs = p.x + (n * C + c) * S;
@@ -252,14 +436,23 @@ __global__ void __launch_bounds__(THREADS) epi_stream_kernel(const EpiParams p) 
     }
     cluster_sync();
   }
+  pdl_trigger();
 }
 
 using EpiKernelFn = void (*)(EpiParams);
 
 static EpiKernelFn epi_kernel(const EpiPlan& plan) {
   if (plan.threads != kEpiThreads) return nullptr;
-  return plan.path == EpiPath::kRange ? &epi_range_kernel<kEpiThreads>
-                                      : &epi_stream_kernel<kEpiThreads>;
+  switch (plan.path) {
+    case EpiPath::kRange:
+      return plan.want_arg ? &epi_range_kernel<kEpiThreads, true>
+                           : &epi_range_kernel<kEpiThreads, false>;
+    case EpiPath::kRangeL2:
+      return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true>
+                           : &epi_range_l2_kernel<kEpiThreads, false>;
+    case EpiPath::kStream: return &epi_stream_kernel<kEpiThreads>;
+  }
+  return nullptr;
 }
 
 static cudaError_t epi_prepare(EpiKernelFn fn, const EpiPlan& plan) {
@@ -305,13 +498,15 @@ cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t str
   cfg.blockDim = dim3(plan.threads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = plan.cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, fn, p);
 }
 

@@ -310,19 +310,20 @@ int epi_query(const void* arg) { return epi_max_active_clusters(static_cast<cons
 
 int epi_capacity(const EpiPlan& plan) {
   char key[128];
-  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%zu", static_cast<int>(plan.path), plan.threads,
-                plan.cluster, plan.smem);
+  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%d|%zu", static_cast<int>(plan.path), plan.threads,
+                plan.cluster, plan.want_arg ? 1 : 0, plan.smem);
   EpiQuery q{plan};
   return occupancy_cached(key, epi_query, &q);
 }
 
-constexpr size_t kEpiTargetBytes = 110 * 1024;   // staged bytes per CTA: two CTAs per SM
+constexpr size_t kEpiTargetBytes = 56 * 1024;   // staged bytes per buffer: two CTAs per SM
 
-// Range plan: cluster of CTAs per sample, each CTA staging a range of
-// positions of all C channels. Preferred cluster sizes in order; the first
-// whose per-CTA staging fits kEpiTargetBytes wins, else the first that fits
-// shared memory at all. FNORM_EPI_CLUSTER forces a size, FNORM_EPI_STREAM the
-// two-read kernel.
+// Range plans: a cluster of CTAs per sample, each CTA owning a range of
+// positions of all C channels. Default: the L2 form (no staging), 4-CTA
+// clusters. FNORM_EPI_STAGED=1 selects the staged (double-buffered shared
+// memory) form: preferred cluster sizes in order, the first whose per-buffer
+// staging fits kEpiTargetBytes wins, else the first that fits shared memory.
+// FNORM_EPI_CLUSTER forces a cluster size, FNORM_EPI_STREAM the fallback.
 fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax, int64_t N,
                            int64_t C, int64_t S, EpiPlan* out) {
   const DeviceInfo& di = device_info();
@@ -332,7 +333,7 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   EpiPlan plan{};
   plan.threads = kEpiThreads;
   bool have = false;
-  if (vec && C <= 1024) {
+  if (vec && C <= 1024 && env("FNORM_EPI_STAGED")) {
     const int cands[] = {8, 16, 4, 2, 1};
     const int64_t nv4 = S / 4;
     for (int pass = 0; pass < 2 && !have; ++pass) {
@@ -344,13 +345,28 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
         const size_t staged = static_cast<size_t>(C) * per * 16;
         if (smem > static_cast<size_t>(di.max_smem_optin) || staged >= (size_t(1) << 20)) continue;
         if (pass == 0 && !force_cl && staged > kEpiTargetBytes) continue;
-        EpiPlan cand{EpiPath::kRange, kEpiThreads, cl_eff, per, smem, 0};
+        EpiPlan cand{EpiPath::kRange, kEpiThreads, cl_eff, per, argmax != nullptr, smem, 0};
         if (epi_capacity(cand) > 0) {
           plan = cand;
           have = true;
           break;
         }
       }
+    }
+  }
+  if (vec && C <= 1024 && !have) {
+    // Default: the range decomposition without staging -- statistics from
+    // HBM, outputs re-read from L2 (4-CTA clusters keep every sample of the
+    // page's shape resident at once).
+    const int cl = force_cl ? std::atoi(force_cl) : 4;
+    const int64_t nv4 = S / 4;
+    const int64_t per = (nv4 + cl - 1) / cl;
+    const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
+    EpiPlan cand{EpiPath::kRangeL2, kEpiThreads, cl_eff, per, argmax != nullptr,
+                 epi_range_l2_smem(C, cl_eff), 0};
+    if (cl >= 1 && cl <= kMaxCluster && epi_capacity(cand) > 0) {
+      plan = cand;
+      have = true;
     }
   }
   if (!have) {
@@ -506,7 +522,7 @@ fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* 
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
   EpiParams p{x, m, y, argmax, N, C, S, eps, clamp_lo, clamp_hi, plan.per,
-              (env("FNORM_DEBUG_FORCE_TIMEOUT") && plan.path == EpiPath::kRange) ? 1 : 0, err};
+              env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0, err};
   return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 

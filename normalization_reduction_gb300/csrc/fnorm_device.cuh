@@ -207,6 +207,19 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel is launched so that it may start
+// while the previous kernel in the stream is finishing; before its first
+// access to global memory a kernel waits until all prerequisite grids have
+// completed and their writes are visible (griddepcontrol.wait), and near its
+// end it lets the next launch begin (griddepcontrol.launch_dependents). Both
+// are no-ops for a kernel launched without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier + TMA bulk copy (cp.async.bulk, non-tensor form: 16-byte aligned
 // addresses, size a multiple of 16), all waits bounded by %globaltimer.
 // ---------------------------------------------------------------------------

@@ -80,13 +80,14 @@ struct EpiParams {
   unsigned* err;
 };
 
-enum class EpiPath : int { kRange = 0, kStream = 1 };
+enum class EpiPath : int { kRange = 0, kStream = 1, kRangeL2 = 2 };
 
 struct EpiPlan {
   EpiPath path;
   int threads;
   int cluster;
   int64_t per;
+  bool want_arg;
   size_t smem;   // dynamic shared memory bytes
   int grid;      // CTAs (multiple of cluster)
 };
@@ -98,6 +99,7 @@ constexpr int kEpiMaxChannels = 8192;
 cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t stream);
 int epi_max_active_clusters(const EpiPlan& plan);
 size_t epi_range_smem(int64_t C, int64_t per, int cluster);
+size_t epi_range_l2_smem(int64_t C, int cluster);
 size_t epi_stream_smem(int64_t C, int cluster);
 
 // ---------------------------------------------------------------- BatchNorm

@@ -36,9 +36,33 @@ namespace fnorm {
 // Exact two-pass statistics of the first `nvalid` values of a thread's slots
 // (values in (k, j) order: slot k, element j). Invalid values are ignored.
 template <class Tin, int NV>
+__device__ __forceinline__ Stat tile_stat_full(const uint4 (&r)[NV]) {
+  using E = Elem<Tin>;
+  constexpr int W = E::W;
+  const float x0 = E::get(r[0], 0);
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int j = 0; j < W; ++j) s[j & 3] += E::get(r[k], j) - x0;
+  constexpr float n = static_cast<float>(NV * W);
+  const float mean = x0 + ((s[0] + s[1]) + (s[2] + s[3])) * (1.0f / n);
+  float q[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+#pragma unroll
+    for (int j = 0; j < W; ++j) {
+      const float d = E::get(r[k], j) - mean;
+      q[j & 3] = fmaf(d, d, q[j & 3]);
+    }
+  return Stat{n, mean, (q[0] + q[1]) + (q[2] + q[3])};
+}
+
+template <class Tin, int NV, bool FAST = true>
 __device__ __forceinline__ Stat tile_stat(const uint4 (&r)[NV], int nvalid) {
   using E = Elem<Tin>;
   constexpr int W = E::W;
+  if (FAST && nvalid == NV * W) return tile_stat_full<Tin, NV>(r);   // no per-value predicates
   if (nvalid <= 0) return stat_empty();
   const float x0 = E::get(r[0], 0);
   float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -153,6 +177,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
     nvalid = first < S ? clamp_int((S - first + THREADS - 1) / THREADS, 0, NV * W) : 0;
   }
 
+  pdl_wait();
   int it = 0;
   for (int64_t q = cid; q < p.NC; q += ncl, ++it) {
     const Tin* xs = x + q * S;
@@ -174,7 +199,9 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
       }
     }
 
-    const Stat cta = cta_merge<THREADS>(tile_stat<Tin, NV>(r, nvalid), warp_part);
+    // (no full-tile fast path here: a second unrolled copy of the two-pass would
+    // push the 64-register budget of 8 bf16 slots per thread into spills)
+    const Stat cta = cta_merge<THREADS>(tile_stat<Tin, NV, false>(r, nvalid), warp_part);
     const float2 mr = cluster_finalize<THREADS>(cta, cta_part, &fin, csize, it, p.eps);
     if (crank == 0 && tid == 0) {
       if (p.mean_out) p.mean_out[q] = mr.x;
@@ -202,6 +229,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
                                (E::get(r[k], j) - mr.x) * mr.y);
     }
   }
+  pdl_trigger();
   // No CTA may leave while another can still read its shared memory.
   if (csize > 1) cluster_sync();
 }
@@ -232,6 +260,7 @@ __global__ void __launch_bounds__(256) in_group_kernel(const InParams p) {
     nvalid_lane = gl < S ? clamp_int((S - gl + G - 1) / G, 0, NV * W) : 0;
   }
 
+  pdl_wait();
   // The loop bound is uniform across the warp, so every lane reaches every
   // shuffle; groups past the end of the tensor carry empty statistics.
   for (int64_t base = warp_id * GPW; base < p.NC; base += nwarps * GPW) {
@@ -285,6 +314,7 @@ __global__ void __launch_bounds__(256) in_group_kernel(const InParams p) {
             Elem<Tout>::store1(ys + (k * W + j) * G + gl, (E::get(r[k], j) - mean) * rstd);
     }
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -336,6 +366,7 @@ __global__ void __launch_bounds__(THREADS) in_stream_kernel(const InParams p) {
   const int64_t ntiles = (S + tile_elems - 1) / tile_elems;
   const int64_t t0 = ntiles * crank / csize, t1 = ntiles * (crank + 1) / csize;
 
+  pdl_wait();
   int it = 0;
   for (int64_t q = cid; q < p.NC; q += ncl, ++it) {
     const Tin* xs = x + q * S;
@@ -380,6 +411,7 @@ __global__ void __launch_bounds__(THREADS) in_stream_kernel(const InParams p) {
       }
     }
   }
+  pdl_trigger();
   if (csize > 1) cluster_sync();
 }
 
@@ -478,6 +510,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
   if (csize > 1) cluster_sync();   // peers' barriers exist before anyone signals them
   else __syncthreads();
 
+  pdl_wait();
   bool failed = false, xfailed = false;
   unsigned tparity = 0;
   if (tid == 0 && sbytes > 0 && cid < p.NC) {
@@ -587,6 +620,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
       for (int k = 0; k < NR; ++k) r[k] = (k < nr_valid) ? ld_v4(xv + k * THREADS) : make_uint4(0, 0, 0, 0);
     }
   }
+  pdl_trigger();
   if (csize > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
   if (failed && sbytes > 0) mbar_wait_bounded(&tma_bar, tparity, p.err);
 }
@@ -602,14 +636,17 @@ static cudaError_t launch_clustered(K kernel, int grid, int threads, int cluster
   cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int nattr = 0;
+  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+  ++nattr;
   if (cluster > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    nattr = 1;
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = cluster;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;

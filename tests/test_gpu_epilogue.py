@@ -50,11 +50,28 @@ def test_page_shape_subset(orc):
     check(orc, x, m, what="page shape")
 
 
+@pytest.mark.parametrize("staged", [False, True], ids=["l2", "staged"])
 @pytest.mark.parametrize("cl", [1, 2, 4, 8, 16])
-def test_cluster_sizes(orc, monkeypatch, cl):
+def test_cluster_sizes(orc, monkeypatch, cl, staged):
+    """Both range kernels (L2 re-read and double-buffered staging) at every
+    cluster size; staged plans that do not fit fall back to the stream kernel."""
     monkeypatch.setenv("FNORM_EPI_CLUSTER", str(cl))
+    if staged:
+        monkeypatch.setenv("FNORM_EPI_STAGED", "1")
     x, m = inputs.epilogue(dev(), shape=(5, 16, 14, 30, 30))
     check(orc, x, m, what=f"cluster {cl}")
+
+
+@pytest.mark.parametrize("shape", [(4, 16, 14, 30, 30), (3, 5, 1000), (2, 1, 4096)])
+def test_staged_shapes(orc, monkeypatch, shape):
+    monkeypatch.setenv("FNORM_EPI_STAGED", "1")
+    x, m = inputs.epilogue(dev(), shape=shape, seed=4321 + shape[1])
+    check(orc, x, m, what=f"staged {shape}")
+
+
+def test_staged_timeout_hook(orc, monkeypatch):
+    monkeypatch.setenv("FNORM_EPI_STAGED", "1")
+    test_bounded_wait_timeout(orc, monkeypatch)
 
 
 @pytest.mark.parametrize("shape", [(3, 1, 64), (2, 3, 100), (4, 5, 12), (2, 7, 1000),
