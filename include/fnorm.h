@@ -139,7 +139,8 @@ FNORM_API size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S)
  *                 time must not share a workspace.
  * Requires N*S >= 2 (the unbiased estimate needs two values).
  * x is read twice (statistics, then normalisation in reverse order so that
- * the tail of the first pass is still in L2) and y written once.
+ * the tail of the first pass is still in L2) and y written once; two kernel
+ * launches.
  */
 FNORM_API fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma, const float* beta,
                                    float scale, float* running_mean, float* running_var,

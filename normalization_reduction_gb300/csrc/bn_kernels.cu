@@ -7,19 +7,22 @@
 //
 // A channel's values are N runs of S contiguous elements, C*S apart. A channel
 // of the page's tensor (128 x 126 x 126 fp32 = 8.1 MB) is far larger than any
-// on-chip store, so x is read twice:
-//   1. bn_stats_kernel   -- one CTA per (run, chunk of <= 16384 elements):
-//                           128-bit loads, exact two-pass per 16-value register
-//                           tile, Chan merges -> one partial (n, mean, M2) per
-//                           CTA in the caller's workspace;
-//   2. bn_finalize_kernel -- one CTA per channel merges its partials in index
-//                           order (deterministic), writes (mean, A, B) with
-//                           y = (x - mean)*A + B, A = scale*gamma*rstd,
-//                           B = scale*beta, the saved statistics and the
-//                           running-statistic update;
-//   3. bn_apply_kernel   -- the normalisation pass, visiting runs in the
-//                           reverse of the statistics pass so the last ~100 MB
-//                           read by pass 1 are still in L2.
+// on-chip store, so x is read twice, in two launches:
+//   1. bn_stats_kernel -- one CTA per (run, chunk of <= 16384 elements):
+//                         128-bit loads (8 per thread in flight), exact
+//                         two-pass per register tile, Chan merges -> one
+//                         partial (n, mean, M2) per CTA in the caller's
+//                         workspace;
+//   2. bn_apply_kernel -- one CTA per (run, chunk), visiting them in the
+//                         reverse of the statistics pass so the last ~100 MB
+//                         it read are still in L2. Each CTA first merges its
+//                         channel's partials in a fixed tree (every CTA of the
+//                         channel obtains bit-identical statistics), forms
+//                         y = (x - mean)*A + B with A = scale*gamma*rstd and
+//                         B = scale*beta, and stores with evict-first hints so
+//                         the output does not push the reusable input out of
+//                         L2. The CTA of run 0, chunk 0 also writes the saved
+//                         statistics and updates the running statistics.
 #include "fnorm_device.cuh"
 #include "fnorm_internal.h"
 #include "in_kernels.cuh"
@@ -60,7 +63,7 @@ __device__ __forceinline__ Stat bn_range_stat(const float* xr, int64_t lo, int64
 }
 
 template <int THREADS, int U, bool VEC>
-__global__ void __launch_bounds__(THREADS) bn_stats_kernel(const BnParams p) {
+__global__ void __launch_bounds__(THREADS, 4) bn_stats_kernel(const BnParams p) {
   __shared__ Stat warp_part[THREADS / 32];
   const int64_t c = blockIdx.y, b = blockIdx.x;
   const int64_t n = b / p.chunks, k = b - n * p.chunks;
@@ -73,41 +76,10 @@ __global__ void __launch_bounds__(THREADS) bn_stats_kernel(const BnParams p) {
   pdl_trigger();
 }
 
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS) bn_finalize_kernel(const BnParams p) {
-  __shared__ Stat warp_part[THREADS / 32];
-  const int64_t c = blockIdx.x;
-  const int64_t P = p.N * p.chunks;
-  const float4* part = p.partials + c * P;
-  pdl_wait();
-  Stat acc = stat_empty();
-  for (int64_t i = threadIdx.x; i < P; i += THREADS) {
-    const float4 v = part[i];
-    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
-  }
-  const Stat s = cta_merge<THREADS>(acc, warp_part);
-  if (threadIdx.x == 0) {
-    const float var = s.m2 / s.n;
-    const float rstd = rsqrtf(var + p.eps);
-    const float g = p.gamma ? p.gamma[c] : 1.f;
-    const float bt = p.beta ? p.beta[c] : 0.f;
-    p.coef[c] = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
-    if (p.save_mean) p.save_mean[c] = s.mean;
-    if (p.save_rstd) p.save_rstd[c] = rstd;
-    if (p.running_mean && p.running_var) {
-      const double cnt = static_cast<double>(p.N) * static_cast<double>(p.S);
-      const double mom = p.momentum;
-      const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
-      p.running_mean[c] =
-          static_cast<float>((1.0 - mom) * p.running_mean[c] + mom * static_cast<double>(s.mean));
-      p.running_var[c] = static_cast<float>((1.0 - mom) * p.running_var[c] + mom * unbiased);
-    }
-  }
-  pdl_trigger();
-}
-
 template <int THREADS, int U, bool VEC>
 __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
+  __shared__ Stat warp_part[THREADS / 32];
+  __shared__ float4 coef;
   // reverse of the statistics pass's block order
   const int64_t nb = static_cast<int64_t>(gridDim.x);
   const int64_t lin = static_cast<int64_t>(gridDim.y) * nb - 1 -
@@ -119,7 +91,38 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
   float* yr = p.y + off;
   const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
   pdl_wait();
-  const float4 cf = p.coef[c];
+
+  // channel statistics: the P partials merged in a fixed order
+  const int64_t P = p.N * p.chunks;
+  const float4* part = p.partials + c * P;
+  Stat acc = stat_empty();
+  for (int64_t i = threadIdx.x; i < P; i += THREADS) {
+    const float4 v = part[i];
+    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
+  }
+  const Stat s = cta_merge<THREADS>(acc, warp_part);
+  if (threadIdx.x == 0) {
+    const float var = s.m2 / s.n;
+    const float rstd = rsqrtf(var + p.eps);
+    const float g = p.gamma ? p.gamma[c] : 1.f;
+    const float bt = p.beta ? p.beta[c] : 0.f;
+    coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
+    if (b == 0) {
+      if (p.save_mean) p.save_mean[c] = s.mean;
+      if (p.save_rstd) p.save_rstd[c] = rstd;
+      if (p.running_mean && p.running_var) {
+        const double cnt = static_cast<double>(p.N) * static_cast<double>(p.S);
+        const double mom = p.momentum;
+        const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
+        p.running_mean[c] = static_cast<float>((1.0 - mom) * p.running_mean[c] +
+                                               mom * static_cast<double>(s.mean));
+        p.running_var[c] = static_cast<float>((1.0 - mom) * p.running_var[c] + mom * unbiased);
+      }
+    }
+  }
+  __syncthreads();
+  const float4 cf = coef;
+
   const int tid = threadIdx.x;
   constexpr int64_t TILE = static_cast<int64_t>(THREADS) * U * 4;
   const int64_t ntiles = (hi - lo + TILE - 1) / TILE;
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
     if (VEC) {
       const int64_t v0 = t / 4 + tid, vend = hi / 4;
       const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
-      float* yv = yr + v0 * 4;
+      float4* yv = reinterpret_cast<float4*>(yr) + v0;
       uint4 r[U];
 #pragma unroll
       for (int k2 = 0; k2 < U; ++k2)
@@ -139,12 +142,12 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
           float o[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) o[j] = fmaf(Elem<float>::get(r[k2], j) - cf.x, cf.y, cf.z);
-          VecStore<float, 4>::run(yv + static_cast<int64_t>(k2) * THREADS * 4, o);
+          __stcs(yv + k2 * THREADS, make_float4(o[0], o[1], o[2], o[3]));
         }
       }
     } else {
       for (int64_t e = t + tid; e < t + TILE && e < hi; e += THREADS)
-        yr[e] = fmaf(__ldg(xr + e) - cf.x, cf.y, cf.z);
+        __stcs(yr + e, fmaf(__ldg(xr + e) - cf.x, cf.y, cf.z));
     }
   }
 }
@@ -167,10 +170,7 @@ static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream
 template <bool VEC>
 static cudaError_t bn_launch_t(const BnParams& p, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
-  cudaError_t e = bn_launch_one(&bn_stats_kernel<kBnThreads, kBnUnroll, VEC>, grid, stream, p);
-  if (e != cudaSuccess) return e;
-  e = bn_launch_one(&bn_finalize_kernel<kBnThreads>, dim3(static_cast<unsigned>(p.C), 1, 1),
-                    stream, p);
+  cudaError_t e = bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, VEC>, grid, stream, p);
   if (e != cudaSuccess) return e;
   return bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, VEC>, grid, stream, p);
 }

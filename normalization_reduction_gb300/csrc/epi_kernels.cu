@@ -32,6 +32,12 @@
 
 namespace fnorm {
 
+// TMA ring form (below): stages in flight per CTA, consumer threads, channels
+// per consumer warp.
+constexpr int kEpiStages = 3;
+constexpr int kEpiRingCons = kEpiRingThreads - 32;   // 8 consumer warps
+constexpr int kEpiRingCpw = kEpiRingMaxC / (kEpiRingCons / 32);
+
 static __host__ __device__ __forceinline__ size_t align128(size_t v) {
   return (v + 127) & ~size_t(127);
 }
@@ -46,6 +52,12 @@ size_t epi_range_smem(int64_t C, int64_t per, int cluster) {
 size_t epi_range_l2_smem(int64_t C, int cluster) {
   return static_cast<size_t>(C) * 16 + 2 * static_cast<size_t>(C) * cluster * 16;
 }
+
+size_t epi_ring_smem(int64_t C, int ring_t, int cluster) {
+  return static_cast<size_t>(kEpiStages) * C * ring_t * 16 + static_cast<size_t>(C) * 16 +
+         2 * static_cast<size_t>(C) * cluster * 16;
+}
+
 
 size_t epi_stream_smem(int64_t C, int cluster) {
   return static_cast<size_t>(C) * 16 + static_cast<size_t>((C + cluster - 1) / cluster) * 16;
@@ -142,8 +154,12 @@ __global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
     const unsigned use_parity = (static_cast<unsigned>(it) >> 1) & 1u;   // k-th use of buffer b
     const uint4* xs = stage_of(b);
     if (seg_bytes > 0 && !failed) {
-      const bool ok = mbar_wait_bounded(&sbar[b], use_parity, p.err);
+      bool ok = true;
+      if (warp == 0) ok = mbar_wait_bounded(&sbar[b], use_parity, p.err);
       failed = __syncthreads_or(!ok) != 0;
+      // the waiting warp observed the completed copies; the others now observe
+      // the same completed phase without spinning
+      if (!failed && warp != 0) mbar_wait_bounded(&sbar[b], use_parity, p.err);
     }
     float4* sl = slots + size_t(b) * C * csize;
     if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
@@ -169,9 +185,11 @@ __global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
       for (unsigned rr = lane; rr < csize; rr += 32)
         st_async_v4(&sl[size_t(c) * csize + crank], &xbar[b], rr, v);
     }
-    // all partials of every channel: merge in rank order
-    if (!xfailed) {
-      const bool ok = mbar_wait_bounded(&xbar[b], use_parity, p.err);
+    // all partials of every channel: merge in rank order (one warp waits)
+    __syncthreads();
+    {
+      bool ok = true;
+      if (warp == 0 && !xfailed) ok = mbar_wait_bounded(&xbar[b], use_parity, p.err);
       if (__syncthreads_or(!ok)) xfailed = true;
     }
     for (int c = warp; c < C; c += NWARP) {
@@ -324,10 +342,12 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       for (unsigned rr = lane; rr < csize; rr += 32)
         st_async_v4(&sl[size_t(c) * csize + crank], &xbar[b], rr, v);
     }
-    if (!xfailed) {
-      const bool ok = mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(it) >> 1) & 1u, p.err);
-      if (__syncthreads_or(!ok)) xfailed = true;
-    }
+    // Warps park at the CTA barrier while one warp waits for the partials.
+    __syncthreads();
+    bool ok = true;
+    if (warp == 0 && !xfailed)
+      ok = mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(it) >> 1) & 1u, p.err);
+    if (__syncthreads_or(!ok)) xfailed = true;
     for (int c = warp; c < C; c += NWARP) {
       Stat s = stat_empty();
       if (lane < static_cast<int>(csize)) {
@@ -366,6 +386,234 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       }
     }
     __syncthreads();   // coefficients consumed before the next sample rewrites them
+  }
+  pdl_trigger();
+  if (csize > 1) cluster_sync();
+  // Test hook, after the last cluster barrier so no peer waits on this CTA:
+  // a wait on a barrier nothing completes must expire, record the timeout in
+  // the error word and return.
+  if (p.debug_timeout && cid == 0 && crank == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
+}
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Range kernel, TMA ring form (FNORM_EPI_RING=1): the range decomposition of the
+// L2 form with all global reads done by the TMA engine. Per CTA, one producer
+// warp streams the CTA's position range of all C channels through a ring of
+// kEpiStages shared-memory stages (C bulk copies per stage, full/empty
+// mbarriers), twice per sample: pass 1 (from HBM) feeds the statistics, pass 2
+// (the same bytes again, mostly from L2) feeds the outputs. Eight consumer
+// warps compute from shared memory. The producer runs ahead of the consumers
+// by up to kEpiStages stages -- into pass 2 while the cluster exchange of the
+// statistics is still in flight, and into the next sample -- so each SM keeps
+// tens of KB of loads in flight at all times without spending registers.
+//   stage = C x T position vectors (16 B), T = ring_t (runtime, <= 256)
+//   pass 1: channel c is reduced by consumer warp c % 8, lanes over vectors;
+//           per-lane Chan accumulators (up to kEpiRingCpw channels per warp)
+//   pass 2: TPV = 256/T consumer threads per position vector, each over the
+//           channels c = h (mod TPV); (max, lowest index) combined by shuffles
+
+__device__ __forceinline__ void epi_combine(float& best, int& arg, float ob, int oa) {
+  if (ob > best || (ob == best && oa < arg)) {
+    best = ob;
+    arg = oa;
+  }
+}
+
+template <bool WANT_ARG>
+__global__ void __launch_bounds__(kEpiRingCons + 32, 2) epi_ring_kernel(const EpiParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kEpiStages];
+  __shared__ __align__(8) uint64_t empty_bar[kEpiStages];
+  __shared__ __align__(8) uint64_t xbar[2];
+  __shared__ __align__(8) uint64_t dbg_bar;
+  constexpr int NCW = kEpiRingCons / 32;    // consumer warps
+
+  const int64_t S = p.S;
+  const int C = static_cast<int>(p.C);
+  const int64_t per = p.per;
+  const int T = p.ring_t;
+  const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
+  const unsigned cid = cluster_id_x(), ncl = ncluster_x();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t stage_vecs = size_t(C) * T;
+  uint4* ring = reinterpret_cast<uint4*>(smem_raw);                                 // [stages][C][T]
+  float4* coef = reinterpret_cast<float4*>(ring + kEpiStages * stage_vecs);          // [C]
+  float4* slots = coef + C;                                                          // [2][C][csize]
+  const int64_t nv4 = S / 4;
+  const int64_t v0 = per * crank;
+  const int vr = static_cast<int>(v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0);
+  const int nch = (vr + T - 1) / T;                      // chunks per pass
+  const int K = cid < p.N ? static_cast<int>((p.N - 1 - cid) / ncl + 1) : 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < kEpiStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], NCW);
+    }
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    mbar_init(&dbg_bar, 1);
+    fence_mbar_init();
+  }
+  if (csize > 1) cluster_sync();
+  else __syncthreads();
+  pdl_wait();
+
+  if (warp == NCW) {
+    // ---------------- producer warp: lane 0 issues, in job order
+    if (lane == 0) {
+      int g = 0;
+      bool failed = false;
+      for (int k = 0; k < K; ++k) {
+        const int64_t n = cid + int64_t(k) * ncl;
+        for (int pass = 0; pass < 2; ++pass) {
+          for (int j = 0; j < nch; ++j, ++g) {
+            const int st = g % kEpiStages;
+            const unsigned use = static_cast<unsigned>(g / kEpiStages);
+            // wait until the consumers released this stage's previous use
+            if (!failed && use > 0 && !mbar_wait_bounded(&empty_bar[st], (use - 1) & 1u, p.err))
+              failed = true;
+            const int tv = (vr - j * T) < T ? (vr - j * T) : T;
+            const unsigned bytes = static_cast<unsigned>(tv) * 16u;
+            if (failed) continue;
+            mbar_arrive_expect_tx(&full_bar[st], bytes * static_cast<unsigned>(C));
+            uint4* dst = ring + st * stage_vecs;
+            const float* src = p.x + n * C * S + (v0 + int64_t(j) * T) * 4;
+            for (int c = 0; c < C; ++c)
+              tma_bulk_g2s(dst + int64_t(c) * T, src + int64_t(c) * S, bytes, &full_bar[st]);
+          }
+        }
+      }
+    }
+    __syncwarp();   // the warp reconverges before the aligned cluster barrier
+  } else {
+    // ---------------- consumer warps
+    int g = 0;
+    bool failed = false;
+    auto acquire = [&](int st, unsigned use) {
+      if (!failed && !mbar_wait_bounded(&full_bar[st], use & 1u, p.err)) failed = true;
+    };
+    auto release = [&](int st) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[st]);
+    };
+    for (int k = 0; k < K; ++k) {
+      const int64_t n = cid + int64_t(k) * ncl;
+      const int b = k & 1;
+      float4* sl = slots + size_t(b) * C * csize;
+      if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
+      // pass 1: statistics
+      Stat acc[kEpiRingCpw];
+#pragma unroll
+      for (int i = 0; i < kEpiRingCpw; ++i) acc[i] = stat_empty();
+      for (int j = 0; j < nch; ++j, ++g) {
+        const int st = g % kEpiStages;
+        acquire(st, static_cast<unsigned>(g / kEpiStages));
+        const int tv = (vr - j * T) < T ? (vr - j * T) : T;
+        const uint4* stg = ring + st * stage_vecs;
+#pragma unroll
+        for (int i = 0; i < kEpiRingCpw; ++i) {
+          const int c = warp + i * NCW;
+          if (c < C) {
+            const uint4* xc = stg + int64_t(c) * T;
+            for (int v = lane; v < tv; v += 32 * 4) {
+              uint4 r[4];
+              int nvalid = 0;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const bool ok = v + u * 32 < tv;
+                r[u] = ok ? xc[v + u * 32] : make_uint4(0, 0, 0, 0);
+                nvalid += ok ? 4 : 0;
+              }
+              acc[i] = chan_merge(acc[i], tile_stat<float, 4>(r, nvalid));
+            }
+          }
+        }
+        release(st);
+      }
+#pragma unroll
+      for (int i = 0; i < kEpiRingCpw; ++i) {
+        const int c = warp + i * NCW;
+        if (c < C) {   // warp-uniform
+          const Stat a = warp_merge<32>(acc[i]);
+          const float4 v = make_float4(__shfl_sync(kFullMask, a.n, 0), __shfl_sync(kFullMask, a.mean, 0),
+                                       __shfl_sync(kFullMask, a.m2, 0), 0.f);
+          for (unsigned rr = lane; rr < csize; rr += 32)
+            st_async_v4(&sl[size_t(c) * csize + crank], &xbar[b], rr, v);
+        }
+      }
+      // every channel's partials from every rank, merged in rank order
+      if (warp == 0 && !failed &&
+          !mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(k) >> 1) & 1u, p.err))
+        failed = true;
+      named_sync(1, kEpiRingCons);
+      for (int c = warp; c < C; c += NCW) {
+        Stat s2 = stat_empty();
+        if (lane < static_cast<int>(csize)) {
+          const float4 v = sl[size_t(c) * csize + lane];
+          s2 = Stat{v.x, v.y, v.z};
+        }
+        s2 = warp_merge<16>(s2);
+        if (lane == 0) coef[c] = epi_out_coef(s2, __ldg(p.m + c), p.eps, p.lo, p.hi);
+      }
+      named_sync(1, kEpiRingCons);
+      // pass 2: outputs
+      const int tpv = kEpiRingCons / T;            // threads per position vector
+      const int vloc = tid / tpv, h = tid - vloc * tpv;
+      for (int j = 0; j < nch; ++j, ++g) {
+        const int st = g % kEpiStages;
+        acquire(st, static_cast<unsigned>(g / kEpiStages));
+        const int tv = (vr - j * T) < T ? (vr - j * T) : T;
+        const uint4* stg = ring + st * stage_vecs;
+        float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        int arg[4] = {C, C, C, C};
+        if (vloc < tv) {
+          for (int c = h; c < C; c += tpv) {
+            const uint4 u = stg[int64_t(c) * T + vloc];
+            const float4 kk = coef[c];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float z = epi_zc(Elem<float>::get(u, q), kk);
+              if (WANT_ARG) {
+                if (z > best[q]) {
+                  best[q] = z;
+                  arg[q] = c;
+                }
+              } else {
+                best[q] = fmaxf(best[q], z);
+              }
+            }
+          }
+        }
+        release(st);
+        // combine the tpv partial results of each vector (consecutive lanes)
+        for (int off = 1; off < tpv; off <<= 1) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float ob = __shfl_xor_sync(kFullMask, best[q], off);
+            if (WANT_ARG) {
+              const int oa = __shfl_xor_sync(kFullMask, arg[q], off);
+              epi_combine(best[q], arg[q], ob, oa);
+            } else {
+              best[q] = fmaxf(best[q], ob);
+            }
+          }
+        }
+        if (h == 0 && vloc < tv) {
+          const int64_t pos = (v0 + int64_t(j) * T + vloc) * 4;
+          __stcs(reinterpret_cast<float4*>(p.y + n * S + pos), make_float4(best[0], best[1], best[2], best[3]));
+          if (WANT_ARG) {
+            longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pos);
+            __stcs(ao, make_longlong2(arg[0], arg[1]));
+            __stcs(ao + 1, make_longlong2(arg[2], arg[3]));
+          }
+        }
+      }
+      named_sync(1, kEpiRingCons);   // coefficients consumed before the next sample
+    }
   }
   pdl_trigger();
   if (csize > 1) cluster_sync();
@@ -442,6 +690,10 @@ __global__ void __launch_bounds__(THREADS) epi_stream_kernel(const EpiParams p) 
 using EpiKernelFn = void (*)(EpiParams);
 
 static EpiKernelFn epi_kernel(const EpiPlan& plan) {
+  if (plan.path == EpiPath::kRing)
+    return plan.threads == kEpiRingThreads
+               ? (plan.want_arg ? &epi_ring_kernel<true> : &epi_ring_kernel<false>)
+               : nullptr;
   if (plan.threads != kEpiThreads) return nullptr;
   switch (plan.path) {
     case EpiPath::kRange:
@@ -450,6 +702,8 @@ static EpiKernelFn epi_kernel(const EpiPlan& plan) {
     case EpiPath::kRangeL2:
       return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true>
                            : &epi_range_l2_kernel<kEpiThreads, false>;
+    case EpiPath::kRing:
+      return plan.want_arg ? &epi_ring_kernel<true> : &epi_ring_kernel<false>;
     case EpiPath::kStream: return &epi_stream_kernel<kEpiThreads>;
   }
   return nullptr;

@@ -310,8 +310,8 @@ int epi_query(const void* arg) { return epi_max_active_clusters(static_cast<cons
 
 int epi_capacity(const EpiPlan& plan) {
   char key[128];
-  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%d|%zu", static_cast<int>(plan.path), plan.threads,
-                plan.cluster, plan.want_arg ? 1 : 0, plan.smem);
+  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%d|%d|%zu", static_cast<int>(plan.path),
+                plan.threads, plan.cluster, plan.want_arg ? 1 : 0, plan.ring_t, plan.smem);
   EpiQuery q{plan};
   return occupancy_cached(key, epi_query, &q);
 }
@@ -320,9 +320,10 @@ constexpr size_t kEpiTargetBytes = 56 * 1024;   // staged bytes per buffer: two 
 
 // Range plans: a cluster of CTAs per sample, each CTA owning a range of
 // positions of all C channels. Default: the L2 form (no staging), 4-CTA
-// clusters. FNORM_EPI_STAGED=1 selects the staged (double-buffered shared
-// memory) form: preferred cluster sizes in order, the first whose per-buffer
-// staging fits kEpiTargetBytes wins, else the first that fits shared memory.
+// clusters. FNORM_EPI_RING=1 selects the TMA ring form (C <= 32);
+// FNORM_EPI_STAGED=1 the staged (double-buffered shared memory) form:
+// preferred cluster sizes in order, the first whose per-buffer staging fits
+// kEpiTargetBytes wins, else the first that fits shared memory.
 // FNORM_EPI_CLUSTER forces a cluster size, FNORM_EPI_STREAM the fallback.
 fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax, int64_t N,
                            int64_t C, int64_t S, EpiPlan* out) {
@@ -345,13 +346,31 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
         const size_t staged = static_cast<size_t>(C) * per * 16;
         if (smem > static_cast<size_t>(di.max_smem_optin) || staged >= (size_t(1) << 20)) continue;
         if (pass == 0 && !force_cl && staged > kEpiTargetBytes) continue;
-        EpiPlan cand{EpiPath::kRange, kEpiThreads, cl_eff, per, argmax != nullptr, smem, 0};
+        EpiPlan cand{EpiPath::kRange, kEpiThreads, cl_eff, per, argmax != nullptr, 0, smem, 0};
         if (epi_capacity(cand) > 0) {
           plan = cand;
           have = true;
           break;
         }
       }
+    }
+  }
+  if (vec && C <= kEpiRingMaxC && !have && env("FNORM_EPI_RING")) {
+    // The TMA ring form (opt-in). Stage = C x T position vectors with
+    // T = 2048 / C rounded down to a power of two in [32, 256] (32 KiB per
+    // stage for C >= 8); 4-CTA clusters unless forced.
+    int T = 256;
+    while (T > 32 && static_cast<int64_t>(T) * C > 2048) T >>= 1;
+    const int cl = force_cl ? std::atoi(force_cl) : 4;
+    const int64_t nv4 = S / 4;
+    const int64_t per = (nv4 + cl - 1) / cl;
+    const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
+    EpiPlan cand{EpiPath::kRing, kEpiRingThreads, cl_eff, per, argmax != nullptr, T,
+                 epi_ring_smem(C, T, cl_eff), 0};
+    if (cl >= 1 && cl <= kMaxCluster && cand.smem <= static_cast<size_t>(di.max_smem_optin) &&
+        epi_capacity(cand) > 0) {
+      plan = cand;
+      have = true;
     }
   }
   if (vec && C <= 1024 && !have) {
@@ -362,7 +381,7 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
     const int64_t nv4 = S / 4;
     const int64_t per = (nv4 + cl - 1) / cl;
     const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
-    EpiPlan cand{EpiPath::kRangeL2, kEpiThreads, cl_eff, per, argmax != nullptr,
+    EpiPlan cand{EpiPath::kRangeL2, kEpiThreads, cl_eff, per, argmax != nullptr, 0,
                  epi_range_l2_smem(C, cl_eff), 0};
     if (cl >= 1 && cl <= kMaxCluster && epi_capacity(cand) > 0) {
       plan = cand;
@@ -382,10 +401,10 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   plan.grid = static_cast<int>(clusters * plan.cluster);
   if (env("FNORM_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d per=%lld smem=%zu grid=%d "
-                 "capacity=%d\n",
+                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d per=%lld ring_t=%d smem=%zu "
+                 "grid=%d capacity=%d\n",
                  static_cast<int>(plan.path), plan.cluster, static_cast<long long>(plan.per),
-                 plan.smem, plan.grid, cap);
+                 plan.ring_t, plan.smem, plan.grid, cap);
   *out = plan;
   return FNORM_OK;
 }
@@ -393,7 +412,7 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
 // ------------------------------------------------------------ BatchNorm
 struct BnLayout {
   int64_t chunk, chunks, P;
-  size_t part_bytes, coef_bytes;
+  size_t part_bytes;
 };
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -404,7 +423,6 @@ BnLayout bn_layout(int64_t N, int64_t C, int64_t S) {
   l.chunks = S > 0 ? (S + l.chunk - 1) / l.chunk : 0;
   l.P = N * l.chunks;
   l.part_bytes = round256(static_cast<size_t>(C) * l.P * 16);
-  l.coef_bytes = round256(static_cast<size_t>(C) * 16);
   return l;
 }
 
@@ -521,8 +539,21 @@ fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* 
   if (st != FNORM_OK) return st;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
-  EpiParams p{x, m, y, argmax, N, C, S, eps, clamp_lo, clamp_hi, plan.per,
-              env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0, err};
+  EpiParams p{};
+  p.x = x;
+  p.m = m;
+  p.y = y;
+  p.argmax = argmax;
+  p.N = N;
+  p.C = C;
+  p.S = S;
+  p.eps = eps;
+  p.lo = clamp_lo;
+  p.hi = clamp_hi;
+  p.per = plan.per;
+  p.debug_timeout = env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0;
+  p.ring_t = plan.ring_t;
+  p.err = err;
   return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -531,7 +562,7 @@ size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S) {
   int64_t t1 = 0, t2 = 0;
   if (!mul_ok(N, C, &t1) || !mul_ok(t1, S, &t2)) return 0;
   const BnLayout l = bn_layout(N, C, S);
-  return l.part_bytes + l.coef_bytes;
+  return l.part_bytes;
 }
 
 fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma, const float* beta,
@@ -557,9 +588,9 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
     return FNORM_ERR_ALIGNMENT;
   const BnLayout l = bn_layout(N, C, S);
   if (l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
-  if (workspace_bytes < l.part_bytes + l.coef_bytes) return FNORM_ERR_INVALID_ARG;
+  if (workspace_bytes < l.part_bytes) return FNORM_ERR_INVALID_ARG;
   const size_t xb = static_cast<size_t>(total) * 4, cb = static_cast<size_t>(C) * 4,
-               wb = l.part_bytes + l.coef_bytes;
+               wb = l.part_bytes;
   if (x != y && overlaps(x, xb, y, xb)) return FNORM_ERR_INVALID_ARG;
   const void* outs[] = {running_mean, running_var, save_mean, save_rstd};
   for (const void* o : outs) {
@@ -588,7 +619,6 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
   p.chunk = l.chunk;
   p.chunks = l.chunks;
   p.partials = static_cast<float4*>(workspace);
-  p.coef = reinterpret_cast<float4*>(static_cast<char*>(workspace) + l.part_bytes);
   p.vec = aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_SCALAR");
   p.err = err;
   return cuda_status(bn_launch(p, reinterpret_cast<cudaStream_t>(stream)));

@@ -77,10 +77,14 @@ struct EpiParams {
   float hi;
   int64_t per;         // position vectors (of 4) per CTA (range path)
   int debug_timeout;   // test hook: wait on an mbarrier nobody completes
+  int ring_t;          // position vectors per ring stage (ring path)
   unsigned* err;
 };
 
-enum class EpiPath : int { kRange = 0, kStream = 1, kRangeL2 = 2 };
+enum class EpiPath : int { kRange = 0, kStream = 1, kRangeL2 = 2, kRangePipe = 3, kRing = 4 };
+constexpr int kEpiRingThreads = 288;   // 8 consumer warps + 1 producer warp
+constexpr int kEpiRingMaxC = 32;       // channels the ring kernel handles
+constexpr int kEpiPipeSetsHost = 4;   // partial-statistics slot sets of the pipelined kernel
 
 struct EpiPlan {
   EpiPath path;
@@ -88,6 +92,7 @@ struct EpiPlan {
   int cluster;
   int64_t per;
   bool want_arg;
+  int ring_t;
   size_t smem;   // dynamic shared memory bytes
   int grid;      // CTAs (multiple of cluster)
 };
@@ -100,6 +105,7 @@ cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t str
 int epi_max_active_clusters(const EpiPlan& plan);
 size_t epi_range_smem(int64_t C, int64_t per, int cluster);
 size_t epi_range_l2_smem(int64_t C, int cluster);
+size_t epi_ring_smem(int64_t C, int ring_t, int cluster);
 size_t epi_stream_smem(int64_t C, int cluster);
 
 // ---------------------------------------------------------------- BatchNorm
@@ -121,13 +127,13 @@ struct BnParams {
   int64_t chunk;        // elements of one (n,c) run one CTA reduces
   int64_t chunks;       // chunks per run
   float4* partials;     // [C][N*chunks] (count, mean, M2, -)
-  float4* coef;         // [C] (mean, A, B, -) with y = (x - mean)*A + B
   bool vec;
   unsigned* err;
 };
 
 constexpr int kBnThreads = 256;
-constexpr int kBnUnroll = 4;
+constexpr int kBnUnroll = 4;        // apply pass: 16-byte loads per thread per tile
+constexpr int kBnStatsUnroll = 8;   // statistics pass
 constexpr int64_t kBnChunk = 16384;   // elements per CTA in the two streaming passes
 
 cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);

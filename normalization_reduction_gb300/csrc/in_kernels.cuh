@@ -239,8 +239,9 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
 // per step. Slot (k, l) of lane l of the group is vector k*G + l of the slice
 // (vector mode) or elements (k*W + j)*G + l.
 // ---------------------------------------------------------------------------
+// Up to 4 slots per lane: 64 registers, four 256-thread CTAs per SM.
 template <class Tin, class Tout, int G, int NV, bool VEC>
-__global__ void __launch_bounds__(256) in_group_kernel(const InParams p) {
+__global__ void __launch_bounds__(256, NV >= 8 ? 2 : 4) in_group_kernel(const InParams p) {
   using E = Elem<Tin>;
   constexpr int W = E::W;
   constexpr int GPW = 32 / G;

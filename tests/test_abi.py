@@ -119,6 +119,6 @@ def test_batchnorm_validation(lib, kw, expect):
 def test_workspace_size(lib):
     assert fn.fnorm_batchnorm_workspace_size(0, 4, 4) == 0
     w = fn.fnorm_batchnorm_workspace_size(128, 64, 126 * 126)
-    assert w % 256 == 0 and w >= 64 * 128 * 16 + 64 * 16
+    assert w % 256 == 0 and w >= 64 * 128 * 16
     # one partial per (run, chunk of up to 16384 elements)
     assert fn.fnorm_batchnorm_workspace_size(2, 3, 40000) >= 3 * 2 * 3 * 16

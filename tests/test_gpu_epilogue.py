@@ -62,11 +62,27 @@ def test_cluster_sizes(orc, monkeypatch, cl, staged):
     check(orc, x, m, what=f"cluster {cl}")
 
 
-@pytest.mark.parametrize("shape", [(4, 16, 14, 30, 30), (3, 5, 1000), (2, 1, 4096)])
-def test_staged_shapes(orc, monkeypatch, shape):
-    monkeypatch.setenv("FNORM_EPI_STAGED", "1")
+@pytest.mark.parametrize("variant", ["FNORM_EPI_STAGED", "FNORM_EPI_RING"])
+@pytest.mark.parametrize("shape", [(4, 16, 14, 30, 30), (3, 5, 1000), (2, 1, 4096), (3, 32, 1000),
+                                   (2, 9, 4)])
+def test_variant_shapes(orc, monkeypatch, shape, variant):
+    """The staged and TMA-ring range kernels on several shapes."""
+    monkeypatch.setenv(variant, "1")
     x, m = inputs.epilogue(dev(), shape=shape, seed=4321 + shape[1])
-    check(orc, x, m, what=f"staged {shape}")
+    check(orc, x, m, what=f"{variant} {shape}")
+
+
+@pytest.mark.parametrize("cl", [1, 2, 4, 8])
+def test_ring_cluster_sizes(orc, monkeypatch, cl):
+    monkeypatch.setenv("FNORM_EPI_RING", "1")
+    monkeypatch.setenv("FNORM_EPI_CLUSTER", str(cl))
+    x, m = inputs.epilogue(dev(), shape=(5, 16, 14, 30, 30))
+    check(orc, x, m, what=f"ring cluster {cl}")
+
+
+def test_ring_timeout_hook(orc, monkeypatch):
+    monkeypatch.setenv("FNORM_EPI_RING", "1")
+    test_bounded_wait_timeout(orc, monkeypatch)
 
 
 def test_staged_timeout_hook(orc, monkeypatch):
