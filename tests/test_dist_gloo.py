@@ -1,0 +1,72 @@
+"""The multi-process host path on the CPU: two gloo ranks shard an
+InstanceNorm and an epilogue workload by slice / sample with no data-path
+collective, and the union of their results equals the single-process result;
+the timing reduction returns the maximum over ranks."""
+import os
+import socket
+
+import numpy as np
+import torch
+import torch.distributed as tdist
+import torch.multiprocessing as mp
+
+from normalization_reduction_gb300 import dist, inputs
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, size, port, outdir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    tdist.init_process_group("gloo", rank=rank, world_size=size)
+    import oracle
+    orc = oracle.get()
+    # InstanceNorm: shard the N*C slices of a small workload of the large shape family
+    x = inputs.instancenorm_large("cpu", shape=(3, 5, 16, 16), seed=77).reshape(15, 256).numpy()
+    lo, hi = dist.shard(15, rank, size)
+    y, _, _ = orc.instancenorm(x[lo:hi])
+    np.save(os.path.join(outdir, f"in_{rank}.npy"), y)
+    # epilogue: shard the samples
+    xe, m = inputs.epilogue("cpu", shape=(5, 4, 2, 3, 4), seed=78)
+    lo, hi = dist.shard(5, rank, size)
+    ye, _, _ = orc.epilogue(xe.numpy()[lo:hi], m.numpy())
+    np.save(os.path.join(outdir, f"epi_{rank}.npy"), ye)
+    # timing reduction
+    got = dist.max_over_ranks(10.0 + rank)
+    np.save(os.path.join(outdir, f"max_{rank}.npy"), np.array([got]))
+    dist.barrier()
+    tdist.destroy_process_group()
+
+
+def test_shard_partitions_exactly():
+    for n in (0, 1, 7, 15, 7168):
+        for size in (1, 2, 3, 8):
+            spans = [dist.shard(n, r, size) for r in range(size)]
+            assert spans[0][0] == 0 and spans[-1][1] == n
+            assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+            sizes = [h - l for l, h in spans]
+            assert max(sizes) - min(sizes) <= 1
+
+
+def test_two_gloo_ranks_match_single_process(tmp_path):
+    size = 2
+    mp.spawn(_worker, args=(size, _free_port(), str(tmp_path)), nprocs=size, join=True)
+    import oracle
+    orc = oracle.get()
+    x = inputs.instancenorm_large("cpu", shape=(3, 5, 16, 16), seed=77).reshape(15, 256).numpy()
+    ref, _, _ = orc.instancenorm(x)
+    got = np.concatenate([np.load(tmp_path / f"in_{r}.npy") for r in range(size)])
+    assert np.array_equal(got, ref)
+    xe, m = inputs.epilogue("cpu", shape=(5, 4, 2, 3, 4), seed=78)
+    refe, _, _ = orc.epilogue(xe.numpy(), m.numpy())
+    gote = np.concatenate([np.load(tmp_path / f"epi_{r}.npy") for r in range(size)])
+    assert np.array_equal(gote, refe)
+    assert all(float(np.load(tmp_path / f"max_{r}.npy")[0]) == 11.0 for r in range(size))
+
+
+def test_max_over_ranks_single_process():
+    assert dist.max_over_ranks(3.5) == 3.5
+    assert dist.world_from_env().size >= 1
