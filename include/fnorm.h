@@ -149,6 +149,38 @@ FNORM_API fnorm_status fnorm_batchnorm_train(const float* x, float* y, const flo
                                    size_t workspace_bytes, fnorm_stream_t stream);
 
 /*
+ * Multi-process (synchronised) training BatchNorm: the batch is split along N
+ * across R processes (one per GPU) and the per-channel statistics are
+ * exchanged once -- the one exchange step of this method
+ * (Kimi-K2.6__l2_p73, blocks 1-2, BatchNorm2d statistics over (N, H, W),
+ * computed here over the union of the shards).
+ *
+ * Step 1, every rank: fnorm_batchnorm_local_stats writes stats_out [C][4]
+ * fp32 (16-byte aligned device memory): per channel (count, mean, M2, 0) of
+ * this rank's shard x [N][C][S], merged in a fixed order. workspace as for
+ * fnorm_batchnorm_train. An empty shard (N*S == 0) writes zeros (the merge
+ * identity).
+ * Step 2, the caller gathers the R arrays in rank order into stats_all
+ * [R][C][4] (e.g. an all-gather over NCCL).
+ * Step 3, every rank: fnorm_batchnorm_apply_stats merges stats_all per
+ * channel in rank order (every rank obtains bit-identical statistics), writes
+ * y = scale * (gamma * (x - mean) * rsqrt(var + eps) + beta) for its shard,
+ * the saved statistics, and updates running_mean/running_var with the merged
+ * count (unbiased estimate; the merged count must be >= 2). Arguments as for
+ * fnorm_batchnorm_train; no workspace. A rank whose shard is empty (N*S == 0)
+ * still merges stats_all and updates its running and saved statistics.
+ */
+FNORM_API fnorm_status fnorm_batchnorm_local_stats(const float* x, float* stats_out, int64_t N,
+                                                   int64_t C, int64_t S, void* workspace,
+                                                   size_t workspace_bytes, fnorm_stream_t stream);
+FNORM_API fnorm_status fnorm_batchnorm_apply_stats(const float* x, float* y, const float* stats_all,
+                                                   int64_t R, const float* gamma, const float* beta,
+                                                   float scale, float* running_mean,
+                                                   float* running_var, float momentum, float eps,
+                                                   float* save_mean, float* save_rstd, int64_t N,
+                                                   int64_t C, int64_t S, fnorm_stream_t stream);
+
+/*
  * fnorm_batchnorm_train without a workspace argument, for callers that cannot
  * allocate device memory: code held to a fixed memory budget reserved up
  * front, plugins whose host owns the allocator and forbids allocation after

@@ -21,7 +21,8 @@ from enum import IntEnum
 __all__ = [
     "FNORM_F32", "FNORM_BF16", "Status", "FnormError", "LIBRARY", "lib",
     "fnorm_instancenorm", "fnorm_instancenorm_epilogue", "fnorm_batchnorm_workspace_size",
-    "fnorm_batchnorm_train", "fnorm_batchnorm_train_noalloc", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
+    "fnorm_batchnorm_train", "fnorm_batchnorm_train_noalloc", "fnorm_batchnorm_local_stats",
+    "fnorm_batchnorm_apply_stats", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
     "instance_norm", "instance_norm_epilogue", "batch_norm_train",
 ]
 
@@ -62,6 +63,9 @@ _SIGNATURES = {
                                _i64, _i64, _vp, ctypes.c_size_t, _vp], _int),
     "fnorm_batchnorm_train_noalloc": ([_vp, _vp, _vp, _vp, _f32, _vp, _vp, _f32, _f32, _vp, _vp,
                                        _i64, _i64, _i64, _vp], _int),
+    "fnorm_batchnorm_local_stats": ([_vp, _vp, _i64, _i64, _i64, _vp, ctypes.c_size_t, _vp], _int),
+    "fnorm_batchnorm_apply_stats": ([_vp, _vp, _vp, _i64, _vp, _vp, _f32, _vp, _vp, _f32, _f32, _vp,
+                                     _vp, _i64, _i64, _i64, _vp], _int),
     "fnorm_status_string": ([_int], ctypes.c_char_p),
     "fnorm_get_last_error": ([], _int),
     "fnorm_version": ([], _int),
@@ -145,6 +149,22 @@ def fnorm_batchnorm_train_noalloc(x, y, gamma, beta, scale, running_mean, runnin
                                                eps, _ptr(save_mean), _ptr(save_rstd), N, C, S,
                                                _stream(stream)),
            "fnorm_batchnorm_train_noalloc")
+
+
+def fnorm_batchnorm_local_stats(x, stats_out, N, C, S, workspace, workspace_bytes,
+                                stream=None) -> None:
+    _check(lib().fnorm_batchnorm_local_stats(_ptr(x), _ptr(stats_out), N, C, S, _ptr(workspace),
+                                             workspace_bytes, _stream(stream)),
+           "fnorm_batchnorm_local_stats")
+
+
+def fnorm_batchnorm_apply_stats(x, y, stats_all, R, gamma, beta, scale, running_mean, running_var,
+                                momentum, eps, save_mean, save_rstd, N, C, S, stream=None) -> None:
+    _check(lib().fnorm_batchnorm_apply_stats(_ptr(x), _ptr(y), _ptr(stats_all), R, _ptr(gamma),
+                                             _ptr(beta), scale, _ptr(running_mean),
+                                             _ptr(running_var), momentum, eps, _ptr(save_mean),
+                                             _ptr(save_rstd), N, C, S, _stream(stream)),
+           "fnorm_batchnorm_apply_stats")
 
 
 def fnorm_status_string(status: int) -> str:

@@ -89,15 +89,18 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
   const int64_t off = (n * p.C + c) * p.S;
   const float* xr = p.x + off;
   float* yr = p.y + off;
-  const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
+  // (an empty shard -- N == 0 -- still merges the statistics and updates the
+  // running statistics, but has nothing to normalise)
+  const int64_t lo = k * p.chunk,
+                hi = p.N == 0 ? lo : ((lo + p.chunk < p.S) ? lo + p.chunk : p.S);
   pdl_wait();
 
-  // channel statistics: the P partials merged in a fixed order
-  const int64_t P = p.N * p.chunks;
-  const float4* part = p.partials + c * P;
+  // channel statistics: the channel's partials (or the ranks' statistics)
+  // merged in a fixed order
+  const float4* part = p.stats + c * p.stats_cstride;
   Stat acc = stat_empty();
-  for (int64_t i = threadIdx.x; i < P; i += THREADS) {
-    const float4 v = part[i];
+  for (int64_t i = threadIdx.x; i < p.stats_count; i += THREADS) {
+    const float4 v = part[i * p.stats_istride];
     acc = chan_merge(acc, Stat{v.x, v.y, v.z});
   }
   const Stat s = cta_merge<THREADS>(acc, warp_part);
@@ -111,7 +114,7 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
       if (p.save_mean) p.save_mean[c] = s.mean;
       if (p.save_rstd) p.save_rstd[c] = rstd;
       if (p.running_mean && p.running_var) {
-        const double cnt = static_cast<double>(p.N) * static_cast<double>(p.S);
+        const double cnt = static_cast<double>(s.n);   // all values of the channel (all ranks)
         const double mom = p.momentum;
         const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
         p.running_mean[c] = static_cast<float>((1.0 - mom) * p.running_mean[c] +
@@ -152,6 +155,24 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
   }
 }
 
+// Local statistics of a rank's shard: one CTA per channel merges the
+// channel's partials in a fixed order into local_out[c] = (n, mean, M2, 0).
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) bn_merge_kernel(const BnParams p) {
+  __shared__ Stat warp_part[THREADS / 32];
+  const int64_t c = blockIdx.x;
+  pdl_wait();
+  const float4* part = p.stats + c * p.stats_cstride;
+  Stat acc = stat_empty();
+  for (int64_t i = threadIdx.x; i < p.stats_count; i += THREADS) {
+    const float4 v = part[i * p.stats_istride];
+    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
+  }
+  const Stat s = cta_merge<THREADS>(acc, warp_part);
+  if (threadIdx.x == 0) p.local_out[c] = make_float4(s.n, s.mean, s.m2, 0.f);
+  pdl_trigger();
+}
+
 // Stream-ordered launch with programmatic dependent launch allowed.
 static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream_t stream,
                                  const BnParams& p) {
@@ -177,6 +198,24 @@ static cudaError_t bn_launch_t(const BnParams& p, cudaStream_t stream) {
 
 cudaError_t bn_launch(const BnParams& p, cudaStream_t stream) {
   return p.vec ? bn_launch_t<true>(p, stream) : bn_launch_t<false>(p, stream);
+}
+
+cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
+  cudaError_t e = p.vec ? bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, true>, grid,
+                                        stream, p)
+                        : bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, false>, grid,
+                                        stream, p);
+  if (e != cudaSuccess) return e;
+  return bn_launch_one(&bn_merge_kernel<kBnThreads>, dim3(static_cast<unsigned>(p.C), 1, 1),
+                       stream, p);
+}
+
+cudaError_t bn_launch_apply(const BnParams& p, cudaStream_t stream) {
+  const int64_t nb = p.N * p.chunks > 0 ? p.N * p.chunks : 1;   // one CTA per channel if empty
+  const dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(p.C), 1);
+  return p.vec ? bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
+               : bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
 }
 
 }  // namespace fnorm

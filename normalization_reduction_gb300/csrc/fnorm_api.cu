@@ -565,63 +565,170 @@ size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S) {
   return l.part_bytes;
 }
 
+namespace {
+
+// Shared validation of the BatchNorm entry points. `need_stats` >= 2: the
+// count N*S must allow the unbiased estimate (single-process training).
+fnorm_status bn_check(const float* x, const float* y, const float* gamma, const float* beta,
+                      float scale, const float* running_mean, const float* running_var,
+                      float momentum, float eps, const float* save_mean, const float* save_rstd,
+                      int64_t N, int64_t C, int64_t S, int64_t* total) {
+  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if (!finite_nonneg(eps) || !std::isfinite(scale) || !std::isfinite(momentum))
+    return FNORM_ERR_INVALID_ARG;
+  if ((running_mean == nullptr) != (running_var == nullptr)) return FNORM_ERR_INVALID_ARG;
+  int64_t NC = 0, NS = 0;
+  if (!mul_ok(N, C, &NC) || !mul_ok(NC, S, total) || !mul_ok(N, S, &NS))
+    return FNORM_ERR_INVALID_ARG;
+  if (C > 65535) return FNORM_ERR_UNSUPPORTED;
+  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4)) ||
+      (running_mean && !aligned(running_mean, 4)) || (running_var && !aligned(running_var, 4)) ||
+      (save_mean && !aligned(save_mean, 4)) || (save_rstd && !aligned(save_rstd, 4)))
+    return FNORM_ERR_ALIGNMENT;
+  if (*total == 0) return FNORM_OK;
+  if (!x || (y == nullptr && (gamma || beta))) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || (y && !aligned(y, 4))) return FNORM_ERR_ALIGNMENT;
+  const size_t xb = static_cast<size_t>(*total) * 4, cb = static_cast<size_t>(C) * 4;
+  if (y && x != y && overlaps(x, xb, y, xb)) return FNORM_ERR_INVALID_ARG;
+  const void* outs[] = {running_mean, running_var, save_mean, save_rstd};
+  for (const void* o : outs)
+    if (overlaps(o, cb, x, xb) || (y && overlaps(o, cb, y, xb))) return FNORM_ERR_INVALID_ARG;
+  return FNORM_OK;
+}
+
+void bn_fill(BnParams* p, const float* x, float* y, const float* gamma, const float* beta,
+             float scale, float* running_mean, float* running_var, float momentum, float eps,
+             float* save_mean, float* save_rstd, int64_t N, int64_t C, int64_t S, unsigned* err) {
+  const BnLayout l = bn_layout(N, C, S);
+  p->x = x;
+  p->y = y;
+  p->gamma = gamma;
+  p->beta = beta;
+  p->scale = scale;
+  p->running_mean = running_mean;
+  p->running_var = running_var;
+  p->momentum = momentum;
+  p->eps = eps;
+  p->save_mean = save_mean;
+  p->save_rstd = save_rstd;
+  p->N = N;
+  p->C = C;
+  p->S = S;
+  p->chunk = l.chunk;
+  p->chunks = l.chunks;
+  p->vec = aligned(x, 16) && (!y || aligned(y, 16)) && S % 4 == 0 && !env("FNORM_FORCE_SCALAR");
+  p->err = err;
+}
+
+}  // namespace
+
 fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma, const float* beta,
                                    float scale, float* running_mean, float* running_var,
                                    float momentum, float eps, float* save_mean, float* save_rstd,
                                    int64_t N, int64_t C, int64_t S, void* workspace,
                                    size_t workspace_bytes, fnorm_stream_t stream) {
-  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
-  if (!finite_nonneg(eps) || !std::isfinite(scale) || !std::isfinite(momentum))
-    return FNORM_ERR_INVALID_ARG;
-  if ((running_mean == nullptr) != (running_var == nullptr)) return FNORM_ERR_INVALID_ARG;
-  int64_t NC = 0, total = 0, NS = 0;
-  if (!mul_ok(N, C, &NC) || !mul_ok(NC, S, &total) || !mul_ok(N, S, &NS))
-    return FNORM_ERR_INVALID_ARG;
-  if (total == 0) return FNORM_OK;
-  if (NS < 2) return FNORM_ERR_INVALID_ARG;   // the unbiased estimate needs two values
-  if (C > 65535) return FNORM_ERR_UNSUPPORTED;
-  if (!x || !y || !workspace) return FNORM_ERR_INVALID_ARG;
-  if (!aligned(x, 4) || !aligned(y, 4) || !aligned(workspace, 256) ||
-      (gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4)) ||
-      (running_mean && !aligned(running_mean, 4)) || (running_var && !aligned(running_var, 4)) ||
-      (save_mean && !aligned(save_mean, 4)) || (save_rstd && !aligned(save_rstd, 4)))
-    return FNORM_ERR_ALIGNMENT;
+  int64_t total = 0;
+  fnorm_status st = bn_check(x, y, gamma, beta, scale, running_mean, running_var, momentum, eps,
+                             save_mean, save_rstd, N, C, S, &total);
+  if (st != FNORM_OK || total == 0) return st;
+  if (N * S < 2) return FNORM_ERR_INVALID_ARG;   // the unbiased estimate needs two values
+  if (!y || !workspace) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FNORM_ERR_ALIGNMENT;
   const BnLayout l = bn_layout(N, C, S);
   if (l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
   if (workspace_bytes < l.part_bytes) return FNORM_ERR_INVALID_ARG;
   const size_t xb = static_cast<size_t>(total) * 4, cb = static_cast<size_t>(C) * 4,
                wb = l.part_bytes;
-  if (x != y && overlaps(x, xb, y, xb)) return FNORM_ERR_INVALID_ARG;
   const void* outs[] = {running_mean, running_var, save_mean, save_rstd};
-  for (const void* o : outs) {
-    if (overlaps(o, cb, x, xb) || overlaps(o, cb, y, xb) || overlaps(o, cb, workspace, wb))
-      return FNORM_ERR_INVALID_ARG;
-  }
+  for (const void* o : outs)
+    if (overlaps(o, cb, workspace, wb)) return FNORM_ERR_INVALID_ARG;
   if (overlaps(workspace, wb, x, xb) || overlaps(workspace, wb, y, xb)) return FNORM_ERR_INVALID_ARG;
 
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
   BnParams p{};
-  p.x = x;
-  p.y = y;
-  p.gamma = gamma;
-  p.beta = beta;
-  p.scale = scale;
-  p.running_mean = running_mean;
-  p.running_var = running_var;
-  p.momentum = momentum;
-  p.eps = eps;
-  p.save_mean = save_mean;
-  p.save_rstd = save_rstd;
-  p.N = N;
-  p.C = C;
-  p.S = S;
-  p.chunk = l.chunk;
-  p.chunks = l.chunks;
+  bn_fill(&p, x, y, gamma, beta, scale, running_mean, running_var, momentum, eps, save_mean,
+          save_rstd, N, C, S, err);
   p.partials = static_cast<float4*>(workspace);
-  p.vec = aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_SCALAR");
-  p.err = err;
+  p.stats = p.partials;
+  p.stats_cstride = l.P;
+  p.stats_istride = 1;
+  p.stats_count = l.P;
   return cuda_status(bn_launch(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fnorm_status fnorm_batchnorm_local_stats(const float* x, float* stats_out, int64_t N, int64_t C,
+                                         int64_t S, void* workspace, size_t workspace_bytes,
+                                         fnorm_stream_t stream) {
+  int64_t total = 0;
+  fnorm_status st = bn_check(x, nullptr, nullptr, nullptr, 1.f, nullptr, nullptr, 0.f, 0.f,
+                             nullptr, nullptr, N, C, S, &total);
+  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if (C == 0) return FNORM_OK;
+  if (!stats_out) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(stats_out, 16)) return FNORM_ERR_ALIGNMENT;
+  if (total == 0) {   // an empty shard contributes the merge identity
+    if (st != FNORM_OK) return st;
+    return cuda_status(cudaMemsetAsync(stats_out, 0, static_cast<size_t>(C) * 16,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+  }
+  if (st != FNORM_OK) return st;
+  if (!workspace) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FNORM_ERR_ALIGNMENT;
+  const BnLayout l = bn_layout(N, C, S);
+  if (l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
+  if (workspace_bytes < l.part_bytes) return FNORM_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(total) * 4, sb = static_cast<size_t>(C) * 16;
+  if (overlaps(stats_out, sb, x, xb) || overlaps(stats_out, sb, workspace, l.part_bytes) ||
+      overlaps(workspace, l.part_bytes, x, xb))
+    return FNORM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  BnParams p{};
+  bn_fill(&p, x, nullptr, nullptr, nullptr, 1.f, nullptr, nullptr, 0.f, 0.f, nullptr, nullptr, N, C,
+          S, err);
+  p.partials = static_cast<float4*>(workspace);
+  p.stats = p.partials;
+  p.stats_cstride = l.P;
+  p.stats_istride = 1;
+  p.stats_count = l.P;
+  p.local_out = reinterpret_cast<float4*>(stats_out);
+  return cuda_status(bn_launch_local_stats(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fnorm_status fnorm_batchnorm_apply_stats(const float* x, float* y, const float* stats_all,
+                                         int64_t R, const float* gamma, const float* beta,
+                                         float scale, float* running_mean, float* running_var,
+                                         float momentum, float eps, float* save_mean,
+                                         float* save_rstd, int64_t N, int64_t C, int64_t S,
+                                         fnorm_stream_t stream) {
+  int64_t total = 0;
+  fnorm_status st = bn_check(x, y, gamma, beta, scale, running_mean, running_var, momentum, eps,
+                             save_mean, save_rstd, N, C, S, &total);
+  if (st != FNORM_OK) return st;
+  if (R < 1 || R > 65536) return FNORM_ERR_INVALID_ARG;
+  // An empty shard still applies the gathered statistics to the running and
+  // saved statistics (every rank of the group updates them alike).
+  const bool stats_only = total == 0 && C > 0 && S >= 0 &&
+                          (running_mean || save_mean || save_rstd);
+  if (total == 0 && !stats_only) return FNORM_OK;
+  if ((!y && !stats_only) || !stats_all) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(stats_all, 16)) return FNORM_ERR_ALIGNMENT;
+  int64_t RC = 0;
+  if (!mul_ok(R, C, &RC)) return FNORM_ERR_INVALID_ARG;
+  const size_t xb = static_cast<size_t>(total) * 4, sb = static_cast<size_t>(RC) * 16;
+  if (overlaps(stats_all, sb, y, xb)) return FNORM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  BnParams p{};
+  bn_fill(&p, x, y, gamma, beta, scale, running_mean, running_var, momentum, eps, save_mean,
+          save_rstd, stats_only ? 0 : N, C, S, err);
+  if (stats_only) p.chunks = 1;
+  p.stats = reinterpret_cast<const float4*>(stats_all);
+  p.stats_cstride = 1;
+  p.stats_istride = C;
+  p.stats_count = R;
+  return cuda_status(bn_launch_apply(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

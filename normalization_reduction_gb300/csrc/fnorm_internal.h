@@ -127,6 +127,14 @@ struct BnParams {
   int64_t chunk;        // elements of one (n,c) run one CTA reduces
   int64_t chunks;       // chunks per run
   float4* partials;     // [C][N*chunks] (count, mean, M2, -)
+  // Statistics the apply pass merges for channel c: stats[c*stats_cstride +
+  // i*stats_istride] for i < stats_count. Local: the partials (cstride =
+  // N*chunks, istride = 1). Multi-rank: gathered [R][C] (cstride 1, istride C).
+  const float4* stats;
+  int64_t stats_cstride;
+  int64_t stats_istride;
+  int64_t stats_count;
+  float4* local_out;    // [C] merged local statistics (local-stats call), else null
   bool vec;
   unsigned* err;
 };
@@ -136,7 +144,9 @@ constexpr int kBnUnroll = 4;        // apply pass: 16-byte loads per thread per 
 constexpr int kBnStatsUnroll = 8;   // statistics pass
 constexpr int64_t kBnChunk = 16384;   // elements per CTA in the two streaming passes
 
-cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);
+cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);          // stats + apply
+cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream);  // stats + merge
+cudaError_t bn_launch_apply(const BnParams& p, cudaStream_t stream);         // apply only
 
 // ---------------------------------------------------------------- helpers
 struct DeviceInfo {

@@ -122,3 +122,31 @@ def test_workspace_size(lib):
     assert w % 256 == 0 and w >= 64 * 128 * 16
     # one partial per (run, chunk of up to 16384 elements)
     assert fn.fnorm_batchnorm_workspace_size(2, 3, 40000) >= 3 * 2 * 3 * 16
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(R=0), fn.Status.ERR_INVALID_ARG),
+    (dict(stats_all=FAKE + (1 << 35) + 4), fn.Status.ERR_ALIGNMENT),
+    (dict(stats_all=0), fn.Status.ERR_INVALID_ARG),
+    (dict(momentum=float("inf")), fn.Status.ERR_INVALID_ARG),
+    (dict(N=0), fn.Status.OK),
+])
+def test_apply_stats_validation(lib, kw, expect):
+    a = dict(x=FAKE, y=FAKE + (1 << 30), stats_all=FAKE + (1 << 35), R=2, gamma=None, beta=None,
+             scale=1.0, running_mean=None, running_var=None, momentum=0.1, eps=1e-5,
+             save_mean=None, save_rstd=None, N=2, C=3, S=64, stream=0)
+    a.update(kw)
+    assert _rc(lambda: fn.fnorm_batchnorm_apply_stats(**a)) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(stats_out=FAKE + (1 << 35) + 8), fn.Status.ERR_ALIGNMENT),
+    (dict(workspace_bytes=16), fn.Status.ERR_INVALID_ARG),
+    (dict(stats_out=FAKE + 64), fn.Status.ERR_INVALID_ARG),      # stats inside x
+    (dict(C=0), fn.Status.OK),
+])
+def test_local_stats_validation(lib, kw, expect):
+    a = dict(x=FAKE, stats_out=FAKE + (1 << 35), N=2, C=3, S=64, workspace=FAKE + (1 << 34),
+             workspace_bytes=1 << 20, stream=0)
+    a.update(kw)
+    assert _rc(lambda: fn.fnorm_batchnorm_local_stats(**a)) == expect

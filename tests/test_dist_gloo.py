@@ -70,3 +70,64 @@ def test_two_gloo_ranks_match_single_process(tmp_path):
 def test_max_over_ranks_single_process():
     assert dist.max_over_ranks(3.5) == 3.5
     assert dist.world_from_env().size >= 1
+
+
+def _chan_merge(a, b):
+    """Pairwise (Chan) merge of (n, mean, M2) rows -- test-side arithmetic."""
+    n = a[0] + b[0]
+    if b[0] == 0:
+        return a
+    if a[0] == 0:
+        return b
+    d = b[1] - a[1]
+    return (n, a[1] + d * b[0] / n, a[2] + b[2] + d * d * a[0] * b[0] / n)
+
+
+def _syncbn_worker(rank, size, port, outdir, splits):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    tdist.init_process_group("gloo", rank=rank, world_size=size)
+    import oracle
+    from normalization_reduction_gb300 import syncbn
+    orc = oracle.get()
+    x, _, _, _, _ = inputs.batchnorm("cpu", shape=(sum(splits), 4, 5, 10), seed=91)
+    lo = sum(splits[:rank])
+    shard = x[lo:lo + splits[rank]].numpy()
+    C, S = 4, 50
+    local = torch.zeros((C, syncbn.STAT_WIDTH), dtype=torch.float32)
+    if splits[rank] * S >= 2:
+        _, _, _, mean, var = orc.batchnorm_train(shard)
+        cnt = splits[rank] * S
+        local[:, 0] = cnt
+        local[:, 1] = torch.from_numpy(mean).float()
+        local[:, 2] = torch.from_numpy(var * cnt).float()
+    gathered = syncbn.gather_rank_stats(local)
+    np.save(os.path.join(outdir, f"gathered_{rank}.npy"), gathered.numpy())
+    np.save(os.path.join(outdir, f"local_{rank}.npy"), local.numpy())
+    tdist.destroy_process_group()
+
+
+def test_syncbn_exchange_gloo(tmp_path):
+    """Three gloo ranks (one with an empty shard) gather per-channel (n, mean, M2)
+    in rank order; merged in that order they give the whole batch's statistics."""
+    splits = [3, 0, 5]
+    size = len(splits)
+    mp.spawn(_syncbn_worker, args=(size, _free_port(), str(tmp_path), splits), nprocs=size,
+             join=True)
+    g = [np.load(tmp_path / f"gathered_{r}.npy") for r in range(size)]
+    loc = [np.load(tmp_path / f"local_{r}.npy") for r in range(size)]
+    for r in range(size):
+        assert g[r].shape == (size, 4, 4)
+        assert np.array_equal(g[r], g[0])              # every rank sees the same array
+        assert np.array_equal(g[0][r], loc[r])         # row r is rank r's statistics
+    import oracle
+    orc = oracle.get()
+    x, _, _, _, _ = inputs.batchnorm("cpu", shape=(sum(splits), 4, 5, 10), seed=91)
+    _, _, _, mean, var = orc.batchnorm_train(x.numpy())
+    for c in range(4):
+        acc = (0.0, 0.0, 0.0)
+        for r in range(size):
+            row = g[0][r, c].astype(np.float64)
+            acc = _chan_merge(acc, (row[0], row[1], row[2]))
+        assert acc[0] == sum(splits) * 50
+        assert abs(acc[1] - mean[c]) <= 1e-6 * max(1.0, abs(mean[c]))
+        assert abs(acc[2] / acc[0] - var[c]) <= 1e-5 * var[c]
