@@ -81,10 +81,9 @@ struct EpiParams {
   unsigned* err;
 };
 
-enum class EpiPath : int { kRange = 0, kStream = 1, kRangeL2 = 2, kRangePipe = 3, kRing = 4 };
+enum class EpiPath : int { kRange = 0, kStream = 1, kRangeL2 = 2, kRing = 4 };
 constexpr int kEpiRingThreads = 288;   // 8 consumer warps + 1 producer warp
 constexpr int kEpiRingMaxC = 32;       // channels the ring kernel handles
-constexpr int kEpiPipeSetsHost = 4;   // partial-statistics slot sets of the pipelined kernel
 
 struct EpiPlan {
   EpiPath path;
