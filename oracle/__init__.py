@@ -1,6 +1,6 @@
 """Oracle for libfnorm -- TEST INFRASTRUCTURE, NOT PRODUCT CODE.
 
-A plain float64, single-threaded CPU statement of the three operations
+A plain float64, single-threaded CPU statement of the library's operations
 (``fnorm_oracle.cpp`` beside this file), wrapped with ctypes and numpy.
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import it. It imports nothing from the CUDA package and the
@@ -95,6 +95,12 @@ class Oracle:
                                                          _f64p, _f64, _f64, _i64, _i64, _i64,
                                                          _f64p, _f64p]
         lib.fnorm_oracle_batchnorm_train_f32.restype = ctypes.c_int
+        lib.fnorm_oracle_instancenorm_affine_f64.argtypes = [_f64p, _f64p, _f64p, _f64p, _i64,
+                                                             _i64, _i64, _f64, _f64p, _f64p]
+        lib.fnorm_oracle_instancenorm_affine_f64.restype = ctypes.c_int
+        lib.fnorm_oracle_batchnorm_eval_f64.argtypes = [_f64p, _f64p, _f64p, _f64p, _f64, _f64p,
+                                                        _f64p, _f64, _i64, _i64, _i64]
+        lib.fnorm_oracle_batchnorm_eval_f64.restype = ctypes.c_int
         self.lib = lib
 
     # -- bf16 storage -----------------------------------------------------
@@ -135,6 +141,27 @@ class Oracle:
         rc = fn(_ptr(x, t), _ptr(y, t), NC, S, float(eps), _ptr(mean, _f64p), _ptr(var, _f64p))
         if rc != 0:
             raise ValueError("oracle instancenorm rejected its arguments")
+        return y, mean, var
+
+    def instancenorm_affine(self, x: np.ndarray, gamma=None, beta=None, eps: float = 1e-5):
+        """x [N, C, *spatial] (any real dtype, taken exactly in float64); gamma/beta
+        [C] or None (1 / 0).
+
+        Returns (y float64 of x's shape, mean [N*C], var [N*C]) in float64.
+        """
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        N, C = x.shape[0], x.shape[1]
+        S = int(np.prod(x.shape[2:])) if x.ndim > 2 else 1
+        g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64).reshape(-1)
+        b = None if beta is None else np.ascontiguousarray(beta, dtype=np.float64).reshape(-1)
+        y = np.empty_like(x)
+        mean = np.empty(N * C, dtype=np.float64)
+        var = np.empty(N * C, dtype=np.float64)
+        rc = self.lib.fnorm_oracle_instancenorm_affine_f64(
+            _ptr(x, _f64p), _ptr(y, _f64p), _ptr(g, _f64p), _ptr(b, _f64p), N, C, S, float(eps),
+            _ptr(mean, _f64p), _ptr(var, _f64p))
+        if rc != 0:
+            raise ValueError("oracle instancenorm_affine rejected its arguments")
         return y, mean, var
 
     # -- fused epilogue ---------------------------------------------------
@@ -186,6 +213,27 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle batchnorm rejected its arguments")
         return y, rm, rv, mean, var
+
+
+    # -- BatchNorm (eval) -------------------------------------------------
+    def batchnorm_eval(self, x: np.ndarray, gamma, beta, scale: float, running_mean,
+                       running_var, eps: float = 1e-5) -> np.ndarray:
+        """x [N, C, *spatial] (taken exactly in float64); gamma/beta [C] or None;
+        running_mean/running_var [C]. Returns y float64 of x's shape."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        N, C = x.shape[0], x.shape[1]
+        S = int(np.prod(x.shape[2:])) if x.ndim > 2 else 1
+        g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64).reshape(-1)
+        b = None if beta is None else np.ascontiguousarray(beta, dtype=np.float64).reshape(-1)
+        rm = np.ascontiguousarray(running_mean, dtype=np.float64).reshape(-1)
+        rv = np.ascontiguousarray(running_var, dtype=np.float64).reshape(-1)
+        y = np.empty_like(x)
+        rc = self.lib.fnorm_oracle_batchnorm_eval_f64(
+            _ptr(x, _f64p), _ptr(y, _f64p), _ptr(g, _f64p), _ptr(b, _f64p), float(scale),
+            _ptr(rm, _f64p), _ptr(rv, _f64p), float(eps), N, C, S)
+        if rc != 0:
+            raise ValueError("oracle batchnorm_eval rejected its arguments")
+        return y
 
 
 _default: Oracle | None = None

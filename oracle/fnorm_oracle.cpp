@@ -231,4 +231,56 @@ int fnorm_oracle_batchnorm_train_f32(const float* x, float* y, const float* gamm
   return 0;
 }
 
+// InstanceNorm with per-channel affine parameters (the module's affine=True
+// option; [p34 block 2] notes the module default is affine=False): for slice
+// q = n*C + c,
+//   y = gamma_c * (x - mean) / sqrt(var + eps) + beta_c,
+// the affine step being the one [p73 block 1] writes for BatchNorm
+// (normalise, multiply by gamma, add beta). gamma/beta (optional, [C]) default
+// to 1 / 0. x and y are [N*C][S] float64; mean_out/var_out as above.
+int fnorm_oracle_instancenorm_affine_f64(const double* x, double* y, const double* gamma,
+                                         const double* beta, int64_t N, int64_t C, int64_t S,
+                                         double eps, double* mean_out, double* var_out) {
+  if (N < 0 || C < 0 || S < 0 || !(eps >= 0.0)) return 1;
+  std::vector<double> v(static_cast<size_t>(S));
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t c = 0; c < C; ++c) {
+      const int64_t q = n * C + c;
+      for (int64_t i = 0; i < S; ++i) v[i] = x[q * S + i];
+      double mean = 0.0, var = 0.0;
+      if (S > 0) moments(v.data(), S, &mean, &var);
+      const double g = gamma ? gamma[c] : 1.0;
+      const double b = beta ? beta[c] : 0.0;
+      for (int64_t i = 0; i < S; ++i) y[q * S + i] = g * normalize(v[i], mean, var, eps) + b;
+      if (mean_out) mean_out[q] = mean;
+      if (var_out) var_out[q] = var;
+    }
+  }
+  return 0;
+}
+
+// Eval-mode BatchNorm followed by a scale factor, [p73 block 1] (in eval mode
+// the module normalises with its running statistics, not the batch's) and
+// [p73 block 2] (the per-channel factor gamma*scale/sqrt(running_var + eps)
+// and shift the pages fold into the convolution): for x [N][C][S],
+//   y = scale * (gamma_c * (x - running_mean_c) / sqrt(running_var_c + eps) + beta_c).
+// Nothing is updated. gamma/beta (optional, [C]) default to 1 / 0.
+int fnorm_oracle_batchnorm_eval_f64(const double* x, double* y, const double* gamma,
+                                    const double* beta, double scale, const double* running_mean,
+                                    const double* running_var, double eps, int64_t N, int64_t C,
+                                    int64_t S) {
+  if (N < 0 || C < 0 || S < 0 || !(eps >= 0.0) || !running_mean || !running_var) return 1;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t c = 0; c < C; ++c) {
+      const double g = gamma ? gamma[c] : 1.0;
+      const double b = beta ? beta[c] : 0.0;
+      const int64_t base = (n * C + c) * S;
+      for (int64_t s = 0; s < S; ++s)
+        y[base + s] =
+            scale * (g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);
+    }
+  }
+  return 0;
+}
+
 }  // extern "C"

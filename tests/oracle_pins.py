@@ -364,4 +364,100 @@ def pin_batchnorm_affine_and_scale(orc):
     assert abs(float(y[1, 0, 1]) - 2.0 * (3.0 * r + 0.5)) <= 4e-7
 
 
+# ---------------------------------------------------------------------------
+# InstanceNorm with per-channel affine parameters
+# ---------------------------------------------------------------------------
+def pin_instancenorm_affine_vs_torch(orc):
+    """torch's float64 instance_norm with weight and bias (an independent
+    library routine) on random slices of several channels and samples."""
+    g = torch.Generator().manual_seed(41)
+    x = torch.randn(3, 5, 4, 7, generator=g, dtype=torch.float64) * 2.0 + 0.7
+    w = torch.randn(5, generator=g, dtype=torch.float64)
+    b = torch.randn(5, generator=g, dtype=torch.float64)
+    ref = F.instance_norm(x, weight=w, bias=b, eps=EPS)
+    y, _, _ = orc.instancenorm_affine(x.numpy(), w.numpy(), b.numpy(), EPS)
+    assert np.max(np.abs(y - ref.numpy())) <= 1e-13
+
+
+def pin_instancenorm_affine_two_valued_closed_form(orc):
+    """A slice alternating a, b has xhat = -+k, k = h/sqrt(h^2 + eps), h = |b-a|/2;
+    channel c then maps it to gamma_c*(-+k) + beta_c, the same for every sample n."""
+    N, C, S = 2, 3, 6
+    a, bb = 1.0, 4.0
+    x = np.tile(np.array([a, bb] * (S // 2)), (N, C, 1))
+    gam = np.array([2.0, -0.5, 3.0])
+    bet = np.array([0.25, 1.0, -2.0])
+    h = abs(bb - a) / 2.0
+    k = h / math.sqrt(h * h + EPS)
+    y, mean, var = orc.instancenorm_affine(x, gam, bet, EPS)
+    for n in range(N):
+        for c in range(C):
+            assert abs(y[n, c, 0] - (gam[c] * -k + bet[c])) <= 1e-15
+            assert abs(y[n, c, 1] - (gam[c] * k + bet[c])) <= 1e-15
+    assert np.all(mean == 2.5) and np.all(var == 2.25)
+
+
+def pin_instancenorm_affine_defaults(orc):
+    """gamma = beta = None is affine=False: the same values as InstanceNorm."""
+    x = np.random.default_rng(43).standard_normal((2, 3, 11))
+    y, _, _ = orc.instancenorm_affine(x, None, None, EPS)
+    ref = F.instance_norm(torch.from_numpy(x), eps=EPS).numpy()
+    assert np.max(np.abs(y - ref)) <= 1e-14
+
+
+# ---------------------------------------------------------------------------
+# BatchNorm in eval mode (running statistics), then the scale factor
+# ---------------------------------------------------------------------------
+def pin_batchnorm_eval_vs_torch(orc):
+    """torch's float64 batch_norm with training=False (running statistics),
+    times the scale factor."""
+    g = torch.Generator().manual_seed(47)
+    x = torch.randn(4, 6, 5, 3, generator=g, dtype=torch.float64) * 1.5 - 0.3
+    rm = torch.randn(6, generator=g, dtype=torch.float64)
+    rv = torch.rand(6, generator=g, dtype=torch.float64) * 3.0 + 0.1
+    w = torch.randn(6, generator=g, dtype=torch.float64)
+    b = torch.randn(6, generator=g, dtype=torch.float64)
+    ref = 2.0 * F.batch_norm(x, rm, rv, weight=w, bias=b, training=False, eps=EPS)
+    y = orc.batchnorm_eval(x.numpy(), w.numpy(), b.numpy(), 2.0, rm.numpy(), rv.numpy(), EPS)
+    assert np.max(np.abs(y - ref.numpy())) <= 1e-13
+
+
+def pin_batchnorm_eval_exact_values(orc):
+    """Hand-computable values (eps chosen so that sqrt(rv + eps) is exact):
+    rv = 3.75, eps = 0.25 -> sqrt = 2; gamma = 3, beta = 0.5, scale = 2,
+    rm = 1: x = 5 -> 2*(3*4/2 + 0.5) = 13; x = -1 -> 2*(3*-1 + 0.5) = -5."""
+    x = np.array([[[5.0, -1.0, 1.0]]])
+    y = orc.batchnorm_eval(x, [3.0], [0.5], 2.0, [1.0], [3.75], 0.25)
+    assert y.tolist() == [[[13.0, -5.0, 1.0]]]
+
+
+def pin_batchnorm_eval_page_folding(orc):
+    """Kimi-K2.6__l2_p73, block 2 folds eval BatchNorm and the scale into a
+    per-channel factor gamma*s/sqrt(rv+eps) and a bias ((b - rm)*gamma/
+    sqrt(rv+eps) + beta)*s of the preceding convolution; with an identity
+    convolution (weight 1, bias 0) that is y = x*factor + bias_c."""
+    rng = np.random.default_rng(53)
+    N, C, S = 3, 4, 9
+    x = rng.standard_normal((N, C, S)) * 3.0
+    gam, bet = rng.standard_normal(C), rng.standard_normal(C)
+    rm, rv = rng.standard_normal(C), rng.uniform(0.2, 2.0, C)
+    s = 2.0
+    factor = gam * s / np.sqrt(rv + EPS)
+    bias = ((0.0 - rm) * gam / np.sqrt(rv + EPS) + bet) * s
+    y = orc.batchnorm_eval(x, gam, bet, s, rm, rv, EPS)
+    assert np.max(np.abs(y - (x * factor[None, :, None] + bias[None, :, None]))) <= 1e-12
+
+
+def pin_batchnorm_eval_equals_train_with_batch_stats(orc):
+    """With the running statistics set to the batch mean and the biased batch
+    variance, the eval form gives the training form's output."""
+    rng = np.random.default_rng(59)
+    x = (rng.standard_normal((5, 3, 8)) * 2.0 + 1.0).astype(np.float32)
+    gam = rng.standard_normal(3).astype(np.float32)
+    bet = rng.standard_normal(3).astype(np.float32)
+    yt, _, _, mean, var = orc.batchnorm_train(x, gam, bet, 2.0, None, None, 0.1, EPS)
+    ye = orc.batchnorm_eval(x, gam, bet, 2.0, mean, var, EPS)
+    assert np.array_equal(ye.astype(np.float32), yt)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -39,6 +39,19 @@ MUTANTS = [
     ("bn_scale_before_beta",
      "static_cast<float>(scale * (g * normalize(v[n * S + s], mean, var, eps) + b));",
      "static_cast<float>(scale * g * normalize(v[n * S + s], mean, var, eps) + b);"),
+    ("in_affine_beta_inside", "y[q * S + i] = g * normalize(v[i], mean, var, eps) + b;",
+     "y[q * S + i] = g * (normalize(v[i], mean, var, eps) + b);"),
+    ("in_affine_swapped", "y[q * S + i] = g * normalize(v[i], mean, var, eps) + b;",
+     "y[q * S + i] = b * normalize(v[i], mean, var, eps) + g;"),
+    ("bn_eval_scale_before_beta",
+     "scale * (g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);",
+     "scale * g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b;"),
+    ("bn_eval_stats_swapped",
+     "scale * (g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);",
+     "scale * (g * normalize(x[base + s], running_var[c], running_mean[c], eps) + b);"),
+    ("bn_eval_dropped_scale",
+     "scale * (g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);",
+     "(g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);"),
     ("bf16_truncate", "const double r = std::nearbyint(q);", "const double r = std::trunc(q);"),
     ("bf16_ties_away", "const double r = std::nearbyint(q);", "const double r = std::round(q);"),
 ]
