@@ -145,6 +145,41 @@ class BatchNorm(Workload):
                                  stream)
 
 
+class InstanceNormAffine(InstanceNormLarge):
+    """InstanceNorm2d(64, affine=True) on x[112,64,512,512]."""
+
+    def __init__(self, dev, shape=inputs.SHAPE_LARGE):
+        self.shape = shape
+        self.name = "instancenorm2d_affine_fp32_" + "x".join(str(v) for v in shape)
+        self.x, self.g, self.b = inputs.instancenorm_affine(dev, shape)
+        self.y = torch.empty_like(self.x)
+        self.N, self.C = shape[0], shape[1]
+        self.S = shape[2] * shape[3]
+
+    def step(self, stream):
+        fn.fnorm_instancenorm_affine(self.x, self.y, self.g, self.b, self.N, self.C, self.S,
+                                     fn.FNORM_F32, fn.FNORM_F32, 1e-5, None, None, stream)
+
+
+class BatchNormEval(Workload):
+    """Eval-mode BatchNorm2d(64) then x*2.0 on x[128,64,126,126]."""
+    name = "batchnorm2d_eval_fp32_128x64x126x126"
+    kernel = "bn_eval_kernel"
+
+    def __init__(self, dev):
+        self.x, self.g, self.b, self.rm, self.rv = inputs.batchnorm_eval(dev)
+        self.y = torch.empty_like(self.x)
+        self.N, self.C = self.x.shape[0], self.x.shape[1]
+        self.S = self.x[0, 0].numel()
+
+    def bytes_per_step(self):
+        return self.x.numel() * 8
+
+    def step(self, stream):
+        fn.fnorm_batchnorm_eval(self.x, self.y, self.g, self.b, 2.0, self.rm, self.rv, 1e-5,
+                                self.N, self.C, self.S, stream)
+
+
 class Sweep(Workload):
     kernel = "in_*_kernel"
     dtype = "bf16"
@@ -244,6 +279,10 @@ def make_workload(args, dev) -> Workload:
         return Epilogue(dev)
     if args.workload == "batchnorm":
         return BatchNorm(dev)
+    if args.workload == "in_affine":
+        return InstanceNormAffine(dev, shape or inputs.SHAPE_LARGE)
+    if args.workload == "bn_eval":
+        return BatchNormEval(dev)
     if args.workload.startswith("sweep:"):
         return Sweep(dev, int(args.workload.split(":")[1]))
     raise SystemExit(f"unknown workload {args.workload}")
@@ -437,7 +476,9 @@ def other_configs(dev, ws, peak):
     """The other workloads, same timing rules (reported alongside)."""
     out = {}
     cases = [("epilogue", lambda: Epilogue(dev), 200, 20),
-             ("batchnorm", lambda: BatchNorm(dev), 20, 5)]
+             ("batchnorm", lambda: BatchNorm(dev), 20, 5),
+             ("batchnorm_eval", lambda: BatchNormEval(dev), 20, 5),
+             ("instancenorm_affine", lambda: InstanceNormAffine(dev), 5, 3)]
     cases += [(f"sweep_S{S}", (lambda S=S: Sweep(dev, S)), 10, 3) for S in inputs.SWEEP_S]
     for key, make, steps, warm in cases:
         wl = make()
@@ -497,7 +538,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip e2e, cpu baseline and the other workloads")
     ap.add_argument("--workload", default="in_large",
-                    help="in_large | epilogue | batchnorm | sweep:S (S a power of 4, 256..4^10)")
+                    help="in_large | in_affine | epilogue | batchnorm | bn_eval | sweep:S "
+                         "(S a power of 4, 256..4^10)")
     ap.add_argument("--shape", default=None,
                     help="N,C,H,W for in_large (e.g. a smaller case for ncu)")
     args = ap.parse_args()

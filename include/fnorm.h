@@ -88,6 +88,24 @@ FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int
                                 float* mean_out, float* rstd_out, fnorm_stream_t stream);
 
 /*
+ * InstanceNorm forward with per-channel affine parameters (the module's
+ * affine = True option; Kimi-K2.6__l1_p34, block 2 notes the default is
+ * affine = False, and Kimi-K2.6__l2_p73, block 1 states the affine step
+ * "normalise, times gamma, plus beta"):
+ *   y = (x - mean) * (rstd * gamma[c]) + beta[c]   for slice q = n*C + c.
+ *
+ *   gamma, beta  optional [C] fp32 device arrays, 4-byte aligned (NULL means
+ *                1 / 0; with both NULL this is fnorm_instancenorm). They may
+ *                not overlap y, mean_out or rstd_out.
+ * Every other argument, the paths and the traffic are those of
+ * fnorm_instancenorm: the parameters add 8 bytes per channel of reads.
+ */
+FNORM_API fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const float* gamma,
+                                       const float* beta, int64_t N, int64_t C, int64_t S,
+                                       fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                       float* mean_out, float* rstd_out, fnorm_stream_t stream);
+
+/*
  * Fused post-convolution epilogue (Kimi-K2.6__l2_p79, block 1: the pipeline
  * scaled = conv_out*m, InstanceNorm over the spatial extent, clamp, a second
  * multiply by m, then the max over the channel dimension), fp32:
@@ -147,6 +165,29 @@ FNORM_API fnorm_status fnorm_batchnorm_train(const float* x, float* y, const flo
                                    float momentum, float eps, float* save_mean, float* save_rstd,
                                    int64_t N, int64_t C, int64_t S, void* workspace,
                                    size_t workspace_bytes, fnorm_stream_t stream);
+
+/*
+ * Eval-mode BatchNorm forward with a trailing scale factor (Kimi-K2.6__l2_p73,
+ * block 1: in eval mode the module normalises with its running statistics;
+ * block 2: the per-channel factor gamma*scale/sqrt(running_var + eps) and
+ * shift that the page folds into the convolution's weights and bias):
+ *
+ *   y = scale * (gamma_c * (x - running_mean_c) * rsqrt(running_var_c + eps)
+ *                + beta_c)
+ *
+ *   x, y          [N][C][S] fp32; y may equal x (in place); any other overlap
+ *                 is rejected.
+ *   gamma, beta   optional [C] fp32 (NULL means 1 and 0).
+ *   running_mean, running_var  required [C] fp32, read only (nothing is
+ *                 updated in eval mode). A negative running_var + eps gives
+ *                 NaN outputs for that channel, as the formula does.
+ * One launch; x is read once and y written once (8 bytes per element).
+ */
+FNORM_API fnorm_status fnorm_batchnorm_eval(const float* x, float* y, const float* gamma,
+                                            const float* beta, float scale,
+                                            const float* running_mean, const float* running_var,
+                                            float eps, int64_t N, int64_t C, int64_t S,
+                                            fnorm_stream_t stream);
 
 /*
  * Multi-process (synchronised) training BatchNorm: the batch is split along N

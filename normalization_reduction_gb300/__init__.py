@@ -20,10 +20,11 @@ from enum import IntEnum
 
 __all__ = [
     "FNORM_F32", "FNORM_BF16", "Status", "FnormError", "LIBRARY", "lib",
-    "fnorm_instancenorm", "fnorm_instancenorm_epilogue", "fnorm_batchnorm_workspace_size",
+    "fnorm_instancenorm", "fnorm_instancenorm_affine", "fnorm_instancenorm_epilogue",
+    "fnorm_batchnorm_workspace_size", "fnorm_batchnorm_eval",
     "fnorm_batchnorm_train", "fnorm_batchnorm_train_noalloc", "fnorm_batchnorm_local_stats",
     "fnorm_batchnorm_apply_stats", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
-    "instance_norm", "instance_norm_epilogue", "batch_norm_train",
+    "instance_norm", "instance_norm_epilogue", "batch_norm_train", "batch_norm_eval",
 ]
 
 LIBRARY = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfnorm.so")
@@ -56,6 +57,10 @@ _int = ctypes.c_int
 # name -> (argtypes, restype)
 _SIGNATURES = {
     "fnorm_instancenorm": ([_vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _vp, _vp, _vp], _int),
+    "fnorm_instancenorm_affine": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _vp,
+                                   _vp, _vp], _int),
+    "fnorm_batchnorm_eval": ([_vp, _vp, _vp, _vp, _f32, _vp, _vp, _f32, _i64, _i64, _i64, _vp],
+                             _int),
     "fnorm_instancenorm_epilogue": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _f32, _vp],
                                     _int),
     "fnorm_batchnorm_workspace_size": ([_i64, _i64, _i64], ctypes.c_size_t),
@@ -119,6 +124,14 @@ def fnorm_instancenorm(x, y, N, C, S, in_dtype, out_dtype, eps=1e-5, mean_out=No
            "fnorm_instancenorm")
 
 
+def fnorm_instancenorm_affine(x, y, gamma, beta, N, C, S, in_dtype, out_dtype, eps=1e-5,
+                              mean_out=None, rstd_out=None, stream=None) -> None:
+    _check(lib().fnorm_instancenorm_affine(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), N, C, S,
+                                           in_dtype, out_dtype, eps, _ptr(mean_out),
+                                           _ptr(rstd_out), _stream(stream)),
+           "fnorm_instancenorm_affine")
+
+
 def fnorm_instancenorm_epilogue(x, m, y, argmax, N, C, S, eps=1e-5, clamp_lo=-1.0, clamp_hi=1.0,
                                 stream=None) -> None:
     _check(lib().fnorm_instancenorm_epilogue(_ptr(x), _ptr(m), _ptr(y), _ptr(argmax), N, C, S,
@@ -128,6 +141,14 @@ def fnorm_instancenorm_epilogue(x, m, y, argmax, N, C, S, eps=1e-5, clamp_lo=-1.
 
 def fnorm_batchnorm_workspace_size(N, C, S) -> int:
     return int(lib().fnorm_batchnorm_workspace_size(N, C, S))
+
+
+def fnorm_batchnorm_eval(x, y, gamma, beta, scale, running_mean, running_var, eps, N, C, S,
+                         stream=None) -> None:
+    _check(lib().fnorm_batchnorm_eval(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), scale,
+                                      _ptr(running_mean), _ptr(running_var), eps, N, C, S,
+                                      _stream(stream)),
+           "fnorm_batchnorm_eval")
 
 
 def fnorm_batchnorm_train(x, y, gamma, beta, scale, running_mean, running_var, momentum, eps,
@@ -195,8 +216,10 @@ def _need_cuda_contig(t, name):
 
 
 def instance_norm(x, eps: float = 1e-5, out_dtype=None, out=None, return_stats: bool = False,
-                  stream=None):
-    """InstanceNorm (affine=False) of x [N, C, *spatial] over the spatial dims."""
+                  stream=None, weight=None, bias=None):
+    """InstanceNorm of x [N, C, *spatial] over the spatial dims; with
+    ``weight``/``bias`` ([C] fp32 CUDA tensors) the affine form
+    y = xhat * weight[c] + bias[c]."""
     import torch
     _need_cuda_contig(x, "x")
     N, C = x.shape[0], x.shape[1]
@@ -209,8 +232,8 @@ def instance_norm(x, eps: float = 1e-5, out_dtype=None, out=None, return_stats: 
     if return_stats:
         mean = torch.empty(N * C, dtype=torch.float32, device=x.device)
         rstd = torch.empty(N * C, dtype=torch.float32, device=x.device)
-    fnorm_instancenorm(x, y, N, C, S, _dtype_code(x.dtype), _dtype_code(y.dtype), eps, mean,
-                       rstd, stream)
+    fnorm_instancenorm_affine(x, y, weight, bias, N, C, S, _dtype_code(x.dtype),
+                              _dtype_code(y.dtype), eps, mean, rstd, stream)
     return (y, mean, rstd) if return_stats else y
 
 
@@ -252,3 +275,18 @@ def batch_norm_train(x, gamma=None, beta=None, running_mean=None, running_var=No
     fnorm_batchnorm_train(x, y, gamma, beta, scale, running_mean, running_var, momentum, eps,
                           save_mean, save_rstd, N, C, S, workspace, workspace.numel(), stream)
     return (y, save_mean, save_rstd) if return_stats else y
+
+
+def batch_norm_eval(x, running_mean, running_var, gamma=None, beta=None, eps: float = 1e-5,
+                    scale: float = 1.0, out=None, stream=None):
+    """Eval-mode BatchNorm of x [N, C, *spatial] fp32 with the running
+    statistics, times ``scale``; nothing is updated."""
+    import torch
+    _need_cuda_contig(x, "x")
+    N, C = x.shape[0], x.shape[1]
+    S = 1
+    for d in x.shape[2:]:
+        S *= d
+    y = out if out is not None else torch.empty_like(x)
+    fnorm_batchnorm_eval(x, y, gamma, beta, scale, running_mean, running_var, eps, N, C, S, stream)
+    return y

@@ -173,6 +173,81 @@ __global__ void __launch_bounds__(THREADS) bn_merge_kernel(const BnParams p) {
   pdl_trigger();
 }
 
+// ---------------------------------------------------------------------------
+// Eval mode (running statistics; page Kimi-K2.6__l2_p73, blocks 1-2): one
+// elementwise pass, y = (x - running_mean_c) * A_c + B_c with
+// A_c = scale * gamma_c * rsqrt(running_var_c + eps) and B_c = scale * beta_c.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 bn_eval_coef(const BnParams& p, int64_t c) {
+  const float rstd = rsqrtf(__ldg(p.running_var + c) + p.eps);
+  const float g = p.gamma ? __ldg(p.gamma + c) : 1.f;
+  const float bt = p.beta ? __ldg(p.beta + c) : 0.f;
+  return make_float4(__ldg(p.running_mean + c), p.scale * g * rstd, p.scale * bt, 0.f);
+}
+
+// Long runs: one CTA per (run, chunk), U vectors per thread in flight.
+template <int THREADS, int U, bool VEC>
+__global__ void __launch_bounds__(THREADS) bn_eval_kernel(const BnParams p) {
+  const int64_t c = blockIdx.y, b = blockIdx.x;
+  const int64_t n = b / p.chunks, k = b - n * p.chunks;
+  const int64_t off = (n * p.C + c) * p.S;
+  const float* xr = p.x + off;
+  float* yr = p.y + off;
+  const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
+  const int tid = threadIdx.x;
+  pdl_wait();
+  const float4 cf = bn_eval_coef(p, c);
+  constexpr int64_t TILE = static_cast<int64_t>(THREADS) * U * 4;
+  for (int64_t t = lo; t < hi; t += TILE) {
+    if (VEC) {
+      const int64_t v0 = t / 4 + tid, vend = hi / 4;
+      const uint4* xv = reinterpret_cast<const uint4*>(xr) + v0;
+      float4* yv = reinterpret_cast<float4*>(yr) + v0;
+      uint4 r[U];
+#pragma unroll
+      for (int k2 = 0; k2 < U; ++k2)
+        if (v0 + k2 * THREADS < vend) r[k2] = ld_v4(xv + k2 * THREADS);
+#pragma unroll
+      for (int k2 = 0; k2 < U; ++k2) {
+        if (v0 + k2 * THREADS < vend) {
+          float o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[j] = fmaf(Elem<float>::get(r[k2], j) - cf.x, cf.y, cf.z);
+          yv[k2 * THREADS] = make_float4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    } else {
+      for (int64_t e = t + tid; e < t + TILE && e < hi; e += THREADS)
+        yr[e] = fmaf(__ldg(xr + e) - cf.x, cf.y, cf.z);
+    }
+  }
+  pdl_trigger();
+}
+
+// Short runs (S < kBnEvalFlatBelow): a grid-stride loop over vectors (or
+// elements), each finding its channel from its index.
+template <int THREADS, bool VEC>
+__global__ void __launch_bounds__(THREADS) bn_eval_flat_kernel(const BnParams p) {
+  const int64_t per_run = VEC ? p.S / 4 : p.S;
+  const int64_t units = p.N * p.C * per_run;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * THREADS;
+  pdl_wait();
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x; u < units;
+       u += stride) {
+    const float4 cf = bn_eval_coef(p, (u / per_run) % p.C);
+    if (VEC) {
+      const uint4 r = ld_v4(reinterpret_cast<const uint4*>(p.x) + u);
+      float o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = fmaf(Elem<float>::get(r, j) - cf.x, cf.y, cf.z);
+      reinterpret_cast<float4*>(p.y)[u] = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+      p.y[u] = fmaf(__ldg(p.x + u) - cf.x, cf.y, cf.z);
+    }
+  }
+  pdl_trigger();
+}
+
 // Stream-ordered launch with programmatic dependent launch allowed.
 static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream_t stream,
                                  const BnParams& p) {
@@ -209,6 +284,22 @@ cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   return bn_launch_one(&bn_merge_kernel<kBnThreads>, dim3(static_cast<unsigned>(p.C), 1, 1),
                        stream, p);
+}
+
+cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream) {
+  if (p.S >= kBnEvalFlatBelow) {
+    const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
+    return p.vec ? bn_launch_one(&bn_eval_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
+                 : bn_launch_one(&bn_eval_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
+  }
+  const int64_t units = p.N * p.C * (p.vec ? p.S / 4 : p.S);
+  const int64_t cap = static_cast<int64_t>(device_info().sm_count) * (2048 / kBnThreads);
+  int64_t blocks = (units + kBnThreads - 1) / kBnThreads;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<unsigned>(blocks), 1, 1);
+  return p.vec ? bn_launch_one(&bn_eval_flat_kernel<kBnThreads, true>, grid, stream, p)
+               : bn_launch_one(&bn_eval_flat_kernel<kBnThreads, false>, grid, stream, p);
 }
 
 cudaError_t bn_launch_apply(const BnParams& p, cudaStream_t stream) {

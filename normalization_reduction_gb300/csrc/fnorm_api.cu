@@ -478,10 +478,12 @@ fnorm_status fnorm_get_last_error(void) {
   return (v & kErrTimeout) ? FNORM_ERR_TIMEOUT : FNORM_OK;
 }
 
-fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
-                                fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
-                                float* mean_out, float* rstd_out, fnorm_stream_t stream) {
+fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const float* gamma,
+                                       const float* beta, int64_t N, int64_t C, int64_t S,
+                                       fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                       float* mean_out, float* rstd_out, fnorm_stream_t stream) {
   if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4))) return FNORM_ERR_ALIGNMENT;
   if ((in_dtype != FNORM_F32 && in_dtype != FNORM_BF16) ||
       (out_dtype != FNORM_F32 && out_dtype != FNORM_BF16))
     return FNORM_ERR_INVALID_ARG;
@@ -503,14 +505,26 @@ fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, in
       overlaps(rstd_out, sb, x, xb) || overlaps(rstd_out, sb, y, yb) ||
       overlaps(mean_out, sb, rstd_out, sb))
     return FNORM_ERR_INVALID_ARG;
+  const size_t cb = static_cast<size_t>(C) * 4;
+  if (overlaps(gamma, cb, y, yb) || overlaps(beta, cb, y, yb) || overlaps(gamma, cb, mean_out, sb) ||
+      overlaps(gamma, cb, rstd_out, sb) || overlaps(beta, cb, mean_out, sb) ||
+      overlaps(beta, cb, rstd_out, sb))
+    return FNORM_ERR_INVALID_ARG;
 
   InPlan plan;
   fnorm_status st = in_make_plan(tin, tout, x, y, NC, S, &plan);
   if (st != FNORM_OK) return st;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
-  const InParams p{x, y, NC, S, eps, mean_out, rstd_out, err};
+  const InParams p{x, y, NC, S, eps, mean_out, rstd_out, err, gamma, beta, C};
   return cuda_status(in_launch_dispatch(tin, tout, p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
+                                fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                float* mean_out, float* rstd_out, fnorm_stream_t stream) {
+  return fnorm_instancenorm_affine(x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype, eps,
+                                   mean_out, rstd_out, stream);
 }
 
 fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
@@ -655,6 +669,26 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
   p.stats_istride = 1;
   p.stats_count = l.P;
   return cuda_status(bn_launch(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fnorm_status fnorm_batchnorm_eval(const float* x, float* y, const float* gamma, const float* beta,
+                                  float scale, const float* running_mean,
+                                  const float* running_var, float eps, int64_t N, int64_t C,
+                                  int64_t S, fnorm_stream_t stream) {
+  if (!running_mean || !running_var) return FNORM_ERR_INVALID_ARG;
+  int64_t total = 0;
+  fnorm_status st = bn_check(x, y, gamma, beta, scale, running_mean, running_var, 0.f, eps,
+                             nullptr, nullptr, N, C, S, &total);
+  if (st != FNORM_OK || total == 0) return st;
+  if (!y) return FNORM_ERR_INVALID_ARG;
+  const BnLayout l = bn_layout(N, C, S);
+  if (S >= kBnEvalFlatBelow && l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  BnParams p{};
+  bn_fill(&p, x, y, gamma, beta, scale, const_cast<float*>(running_mean),
+          const_cast<float*>(running_var), 0.f, eps, nullptr, nullptr, N, C, S, err);
+  return cuda_status(bn_launch_eval(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fnorm_status fnorm_batchnorm_local_stats(const float* x, float* stats_out, int64_t N, int64_t C,

@@ -21,6 +21,9 @@ struct InParams {
   float* mean_out;
   float* rstd_out;
   unsigned* err;
+  const float* gamma;   // [C] per-channel scale (nullptr: 1)
+  const float* beta;    // [C] per-channel shift (nullptr: 0)
+  int64_t C;            // channels: slice q belongs to channel q % C
 };
 
 enum class InPath : int {
@@ -146,6 +149,8 @@ constexpr int64_t kBnChunk = 16384;   // elements per CTA in the two streaming p
 cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);          // stats + apply
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream);  // stats + merge
 cudaError_t bn_launch_apply(const BnParams& p, cudaStream_t stream);         // apply only
+cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream);          // eval mode, one pass
+constexpr int64_t kBnEvalFlatBelow = 1024;   // runs shorter than this take the flat eval kernel
 
 // ---------------------------------------------------------------- helpers
 struct DeviceInfo {

@@ -137,6 +137,18 @@ __device__ __forceinline__ float2 cluster_finalize(const Stat& cta, Stat* cta_pa
   return *fin;
 }
 
+// Output coefficients of slice q: y = (x - mean) * a + b, with a = rstd * gamma_c
+// and b = beta_c for the affine form and a = rstd, b = 0 without it.
+__device__ __forceinline__ float2 in_affine(const InParams& p, int64_t q, float rstd) {
+  float a = rstd, b = 0.f;
+  if (p.gamma != nullptr || p.beta != nullptr) {
+    const int64_t c = q % p.C;
+    if (p.gamma != nullptr) a = rstd * __ldg(p.gamma + c);
+    if (p.beta != nullptr) b = __ldg(p.beta + c);
+  }
+  return make_float2(a, b);
+}
+
 // ---------------------------------------------------------------------------
 // Resident: one CTA (cluster size 1) or one cluster per slice.
 // Slot (k, t) of CTA rank r is vector r*THREADS*NV + k*THREADS + t of the
@@ -207,6 +219,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
       if (p.mean_out) p.mean_out[q] = mr.x;
       if (p.rstd_out) p.rstd_out[q] = mr.y;
     }
+    const float2 ab = in_affine(p, q, mr.y);
 
     if (VEC) {
       Tout* yv = ys + first * W;
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
         if (k * W < nvalid) {
           float o[W];
 #pragma unroll
-          for (int j = 0; j < W; ++j) o[j] = (E::get(r[k], j) - mr.x) * mr.y;
+          for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y);
           VecStore<Tout, W>::run(yv + static_cast<int64_t>(k) * THREADS * W, o);
         }
       }
@@ -226,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
         for (int j = 0; j < W; ++j)
           if (k * W + j < nvalid)
             Elem<Tout>::store1(ys + first + static_cast<int64_t>(k * W + j) * THREADS,
-                               (E::get(r[k], j) - mr.x) * mr.y);
+                               fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y));
     }
   }
   pdl_trigger();
@@ -295,6 +308,7 @@ __global__ void __launch_bounds__(256, NV >= 8 ? 2 : 4) in_group_kernel(const In
       if (p.mean_out) p.mean_out[q] = mean;
       if (p.rstd_out) p.rstd_out[q] = rstd;
     }
+    const float2 ab = in_affine(p, q, rstd);
     Tout* ys = y + q * S;
     if (VEC) {
 #pragma unroll
@@ -302,7 +316,7 @@ __global__ void __launch_bounds__(256, NV >= 8 ? 2 : 4) in_group_kernel(const In
         if (k * W < nvalid) {
           float o[W];
 #pragma unroll
-          for (int j = 0; j < W; ++j) o[j] = (E::get(r[k], j) - mean) * rstd;
+          for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(r[k], j) - mean, ab.x, ab.y);
           VecStore<Tout, W>::run(ys + static_cast<int64_t>(k * G + gl) * W, o);
         }
       }
@@ -312,7 +326,7 @@ __global__ void __launch_bounds__(256, NV >= 8 ? 2 : 4) in_group_kernel(const In
 #pragma unroll
         for (int j = 0; j < W; ++j)
           if (k * W + j < nvalid)
-            Elem<Tout>::store1(ys + (k * W + j) * G + gl, (E::get(r[k], j) - mean) * rstd);
+            Elem<Tout>::store1(ys + (k * W + j) * G + gl, fmaf(E::get(r[k], j) - mean, ab.x, ab.y));
     }
   }
   pdl_trigger();
@@ -385,6 +399,7 @@ __global__ void __launch_bounds__(THREADS) in_stream_kernel(const InParams p) {
       if (p.mean_out) p.mean_out[q] = mr.x;
       if (p.rstd_out) p.rstd_out[q] = mr.y;
     }
+    const float2 ab = in_affine(p, q, mr.y);
     for (int64_t t = t1 - 1; t >= t0; --t) {
       uint4 r[U];
       int nvalid;
@@ -396,7 +411,7 @@ __global__ void __launch_bounds__(THREADS) in_stream_kernel(const InParams p) {
           if (k * W < nvalid) {
             float o[W];
 #pragma unroll
-            for (int j = 0; j < W; ++j) o[j] = (E::get(r[k], j) - mr.x) * mr.y;
+            for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y);
             VecStore<Tout, W>::run(yv + static_cast<int64_t>(k) * THREADS * W, o);
           }
         }
@@ -408,7 +423,7 @@ __global__ void __launch_bounds__(THREADS) in_stream_kernel(const InParams p) {
           for (int j = 0; j < W; ++j)
             if (k * W + j < nvalid)
               Elem<Tout>::store1(ys + e0 + static_cast<int64_t>(k * W + j) * THREADS,
-                                 (E::get(r[k], j) - mr.x) * mr.y);
+                                 fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y));
       }
     }
   }
@@ -585,6 +600,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
       if (p.mean_out) p.mean_out[q] = mr.x;
       if (p.rstd_out) p.rstd_out[q] = mr.y;
     }
+    const float2 ab = in_affine(p, q, mr.y);
     Tout* yq = y + q * S;
     // staged part
 #pragma unroll
@@ -593,7 +609,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
         const uint4 v = stage[k * THREADS + tid];
         float o[W];
 #pragma unroll
-        for (int j = 0; j < W; ++j) o[j] = (E::get(v, j) - mr.x) * mr.y;
+        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(v, j) - mr.x, ab.x, ab.y);
         VecStore<Tout, W>::run(yq + (base + int64_t(k) * THREADS + tid) * W, o);
       }
     }
@@ -611,7 +627,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
       if (k < nr_valid) {
         float o[W];
 #pragma unroll
-        for (int j = 0; j < W; ++j) o[j] = (E::get(r[k], j) - mr.x) * mr.y;
+        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y);
         VecStore<Tout, W>::run(yq + (rbase + int64_t(k) * THREADS) * W, o);
       }
     }

@@ -13,6 +13,12 @@ Workloads (all NCHW / NCDHW contiguous, fp32 unless stated):
 * ``batchnorm``            x[128,64,126,126] per-channel as above;
   gamma = 1 + 0.1 N(0,1), beta = 0.1 N(0,1), running_mean = 0, running_var = 1
   -- the Conv2d output of the page Kimi-K2.6__l2_p73.
+* ``instancenorm_affine``  x as ``instancenorm_large`` (seed 1006) with
+  per-channel gamma = 1 + 0.1 N(0,1), beta = 0.1 N(0,1) -- InstanceNorm2d(64)
+  with its affine=True option.
+* ``batchnorm_eval``       x as ``batchnorm`` (seed 1007) with gamma/beta as
+  there and running statistics of a model that has seen such data:
+  running_mean = mu_c + 0.05 N(0,1), running_var = s_c^2 * U(0.8, 1.2).
 * ``instancenorm_sweep``   bf16 x ~ N(3,2) (rounded from fp32), N = 8,
   2^30 elements in total, slice length S from 256 to 1,048,576.
 
@@ -30,6 +36,8 @@ SEED_LARGE = 1002
 SEED_EPILOGUE = 1003
 SEED_BATCHNORM = 1004
 SEED_SWEEP = 1005
+SEED_AFFINE = 1006
+SEED_BN_EVAL = 1007
 
 SHAPE_SMALL = (2, 4, 16, 16)
 SHAPE_LARGE = (112, 64, 512, 512)
@@ -123,3 +131,29 @@ def instancenorm_sweep(S: int, device="cuda", total: int = SWEEP_TOTAL, N: int =
     k = SWEEP_S.index(S) if (seed is None and S in SWEEP_S) else 0
     return normal(sweep_shape(S, total, N), SEED_SWEEP + k if seed is None else seed, device,
                   mean=3.0, std=2.0, dtype=torch.bfloat16)
+
+
+def channel_affine(C: int, seed: int, device="cpu"):
+    """gamma = 1 + 0.1 N(0,1), beta = 0.1 N(0,1), drawn per channel on the CPU."""
+    gp = _gen(seed + 300_000, "cpu")
+    gamma = 1.0 + 0.1 * torch.randn(C, generator=gp)
+    beta = 0.1 * torch.randn(C, generator=gp)
+    return gamma.to(device), beta.to(device)
+
+
+def instancenorm_affine(device="cuda", shape=SHAPE_LARGE, seed: int = SEED_AFFINE):
+    """Returns (x, gamma [C], beta [C]) on ``device``."""
+    x = normal(shape, seed, device)
+    gamma, beta = channel_affine(shape[1], seed, device)
+    return x, gamma, beta
+
+
+def batchnorm_eval(device="cuda", shape=SHAPE_BATCHNORM, seed: int = SEED_BN_EVAL):
+    """Returns (x, gamma, beta, running_mean, running_var) on ``device``."""
+    x, mu, s = per_channel_normal(shape, seed, device)
+    C = shape[1]
+    gamma, beta = channel_affine(C, seed, "cpu")
+    gr = _gen(seed + 400_000, "cpu")
+    rm = mu + 0.05 * torch.randn(C, generator=gr)
+    rv = s * s * (0.8 + 0.4 * torch.rand(C, generator=gr))
+    return x, gamma.to(device), beta.to(device), rm.to(device), rv.to(device)

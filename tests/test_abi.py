@@ -150,3 +150,40 @@ def test_local_stats_validation(lib, kw, expect):
              workspace_bytes=1 << 20, stream=0)
     a.update(kw)
     assert _rc(lambda: fn.fnorm_batchnorm_local_stats(**a)) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(gamma=FAKE + (1 << 36) + 2), fn.Status.ERR_ALIGNMENT),
+    (dict(beta=FAKE + (1 << 36) + 1), fn.Status.ERR_ALIGNMENT),
+    (dict(gamma=FAKE + (1 << 30) + 8), fn.Status.ERR_INVALID_ARG),   # gamma inside y
+    (dict(beta=FAKE + (1 << 30)), fn.Status.ERR_INVALID_ARG),        # beta inside y
+    (dict(eps=-1.0), fn.Status.ERR_INVALID_ARG),
+    (dict(N=0), fn.Status.OK),
+])
+def test_instancenorm_affine_validation(lib, kw, expect):
+    a = dict(x=FAKE, y=FAKE + (1 << 30), gamma=FAKE + (1 << 36), beta=FAKE + (1 << 36) + 4096,
+             N=2, C=3, S=64, in_dtype=fn.FNORM_F32, out_dtype=fn.FNORM_F32, eps=1e-5,
+             mean_out=None, rstd_out=None, stream=0)
+    a.update(kw)
+    assert _rc(lambda: fn.fnorm_instancenorm_affine(**a)) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(running_mean=None), fn.Status.ERR_INVALID_ARG),         # running statistics required
+    (dict(running_var=None), fn.Status.ERR_INVALID_ARG),
+    (dict(running_var=FAKE + (1 << 33) + 4098), fn.Status.ERR_ALIGNMENT),
+    (dict(y=None), fn.Status.ERR_INVALID_ARG),
+    (dict(y=FAKE + 4), fn.Status.ERR_INVALID_ARG),                # partial overlap with x
+    (dict(running_mean=FAKE + 64), fn.Status.ERR_INVALID_ARG),    # statistics inside x
+    (dict(scale=float("nan")), fn.Status.ERR_INVALID_ARG),
+    (dict(eps=float("inf")), fn.Status.ERR_INVALID_ARG),
+    (dict(C=70000), fn.Status.ERR_UNSUPPORTED),
+    (dict(N=0), fn.Status.OK),
+    (dict(S=0), fn.Status.OK),
+])
+def test_batchnorm_eval_validation(lib, kw, expect):
+    a = dict(x=FAKE, y=FAKE + (1 << 30), gamma=None, beta=None, scale=2.0,
+             running_mean=FAKE + (1 << 33), running_var=FAKE + (1 << 33) + 4096, eps=1e-5,
+             N=2, C=3, S=64, stream=0)
+    a.update(kw)
+    assert _rc(lambda: fn.fnorm_batchnorm_eval(**a)) == expect

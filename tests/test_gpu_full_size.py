@@ -10,6 +10,8 @@ times (the library's default plan):
   saved statistics against the oracle.
 * bf16 sweep, 2^30 elements for each slice length S = 4^4 ... 4^10: 16
   sampled slices per S against the oracle.
+* Affine InstanceNorm fp32 x[112,64,512,512]: 16 sampled slices.
+* Eval BatchNorm fp32 x[128,64,126,126]: five sampled samples n.
 """
 import numpy as np
 import pytest
@@ -105,3 +107,44 @@ def test_sweep_full_size(orc, S):
     assert_close(to_f64(ys), ref, torch.bfloat16, f"C5 S={S}")
     del x, y
     torch.cuda.empty_cache()
+
+
+def test_instancenorm_affine_full_size(orc):
+    """Affine InstanceNorm fp32 x[112,64,512,512] with per-channel gamma/beta:
+    16 sampled slices against the oracle (channel q % 64 for slice q)."""
+    x, gamma, beta = inputs.instancenorm_affine(dev())
+    N, C, H, W = x.shape
+    NC, S = N * C, H * W
+    y = torch.empty_like(x)
+    fn.fnorm_instancenorm_affine(x, y, gamma, beta, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS,
+                                 None, None)
+    torch.cuda.synchronize()
+    idx = sample_slices(NC, 16, 11)
+    ti = torch.from_numpy(idx).to(dev())
+    xs = x.view(NC, S).index_select(0, ti).cpu().numpy().astype(np.float64)
+    ys = y.view(NC, S).index_select(0, ti).cpu().numpy()
+    g, b = gamma.cpu().numpy(), beta.cpu().numpy()
+    for row, q in enumerate(idx):
+        c = int(q) % C
+        ref, _, _ = orc.instancenorm_affine(xs[row].reshape(1, 1, S), g[c:c + 1], b[c:c + 1], EPS)
+        assert_close(ys[row], ref.reshape(S), torch.float32, f"affine slice {q}")
+    del x, y
+    torch.cuda.empty_cache()
+
+
+def test_batchnorm_eval_full_size(orc):
+    """Eval BatchNorm fp32 x[128,64,126,126] with running statistics: samples
+    n = 0, 1, 63, 126, 127 against the oracle, whole output finite."""
+    x, g, b, rm, rv = inputs.batchnorm_eval(dev())
+    N, C = x.shape[0], x.shape[1]
+    S = x[0, 0].numel()
+    y = torch.empty_like(x)
+    fn.fnorm_batchnorm_eval(x, y, g, b, 2.0, rm, rv, EPS, N, C, S)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y).all())
+    pick = torch.tensor([0, 1, 63, 126, 127], device=dev())
+    xs = x.index_select(0, pick).cpu().numpy().reshape(5, C, S)
+    ref = orc.batchnorm_eval(xs, g.cpu().numpy(), b.cpu().numpy(), 2.0, rm.cpu().numpy(),
+                             rv.cpu().numpy(), EPS)
+    assert_close(y.index_select(0, pick).cpu().numpy().reshape(5, C, S), ref, torch.float32,
+                 "eval BN")
