@@ -62,17 +62,80 @@ __device__ __forceinline__ Stat bn_range_stat(const float* xr, int64_t lo, int64
   return acc;
 }
 
+// Units (run, chunk) in memory order: unit m covers chunk m % chunks of run
+// m / chunks = n*C + c. Its partial goes to partials[c][n*chunks + k].
+struct BnUnit {
+  int64_t run, n, c, k, lo, hi;
+};
+__device__ __forceinline__ BnUnit bn_unit(const BnParams& p, int64_t m) {
+  BnUnit u;
+  u.run = m / p.chunks;
+  u.k = m - u.run * p.chunks;
+  u.n = u.run / p.C;
+  u.c = u.run - u.n * p.C;
+  u.lo = u.k * p.chunk;
+  u.hi = (u.lo + p.chunk < p.S) ? u.lo + p.chunk : p.S;
+  return u;
+}
+__device__ __forceinline__ float4* bn_partial(const BnParams& p, const BnUnit& u) {
+  return p.partials + u.c * (p.N * p.chunks) + u.n * p.chunks + u.k;
+}
+
 template <int THREADS, int U, bool VEC>
 __global__ void __launch_bounds__(THREADS, 4) bn_stats_kernel(const BnParams p) {
   __shared__ Stat warp_part[THREADS / 32];
-  const int64_t c = blockIdx.y, b = blockIdx.x;
-  const int64_t n = b / p.chunks, k = b - n * p.chunks;
-  const float* xr = p.x + (n * p.C + c) * p.S;
-  const int64_t lo = k * p.chunk, hi = (lo + p.chunk < p.S) ? lo + p.chunk : p.S;
+  const BnUnit u = bn_unit(p, static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x);
+  const float* xr = p.x + u.run * p.S;
   pdl_wait();
-  const Stat cta = cta_merge<THREADS>(bn_range_stat<THREADS, U, VEC>(xr, lo, hi), warp_part);
-  if (threadIdx.x == 0)
-    p.partials[c * (p.N * p.chunks) + b] = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+  const Stat cta = cta_merge<THREADS>(bn_range_stat<THREADS, U, VEC>(xr, u.lo, u.hi), warp_part);
+  if (threadIdx.x == 0) *bn_partial(p, u) = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+  pdl_trigger();
+}
+
+// Statistics pass in vector mode for units of up to kBnChunk values: the
+// whole unit is in flight at once -- the first THREADS*NR vectors by 128-bit
+// register loads, the rest by one TMA bulk copy into shared memory issued
+// first -- so that four CTAs per SM keep ~256 KB of reads outstanding. Each
+// thread takes the exact two-pass statistics of its register values, then of
+// its staged values, and merges the two.
+template <int THREADS, int NR, int NS>
+__global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnParams p) {
+  extern __shared__ __align__(16) uint4 stage[];   // (THREADS * NS) vectors
+  __shared__ Stat warp_part[THREADS / 32];
+  __shared__ uint64_t bar;
+  const int tid = threadIdx.x;
+  const BnUnit u = bn_unit(p, static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x);
+  const uint4* xv = reinterpret_cast<const uint4*>(p.x + u.run * p.S + u.lo);
+  constexpr int RV = THREADS * NR;
+  const int nvec = static_cast<int>((u.hi - u.lo) / 4);
+  const int svec = nvec > RV ? nvec - RV : 0;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (tid == 0 && svec > 0) {
+    mbar_arrive_expect_tx(&bar, static_cast<unsigned>(svec) * 16u);
+    tma_bulk_g2s(stage, xv + RV, static_cast<unsigned>(svec) * 16u, &bar);
+  }
+  const int rvec = nvec < RV ? nvec : RV;
+  const int kr = tid < rvec ? clamp_int((rvec - tid + THREADS - 1) / THREADS, 0, NR) : 0;
+  uint4 r[NR];
+#pragma unroll
+  for (int k = 0; k < NR; ++k) r[k] = k < kr ? ld_v4(xv + k * THREADS + tid) : make_uint4(0, 0, 0, 0);
+  Stat st = tile_stat<float, NR>(r, kr * 4);
+  if (svec > 0) {
+    // a wait that gives up has flagged the error; it is retried once (bounded)
+    // so that the copy is not in flight when the CTA leaves
+    if (!mbar_wait_bounded(&bar, 0, p.err)) mbar_wait_bounded(&bar, 0, p.err);
+    const int ks = tid < svec ? clamp_int((svec - tid + THREADS - 1) / THREADS, 0, NS) : 0;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) r[k] = k < ks ? stage[k * THREADS + tid] : make_uint4(0, 0, 0, 0);
+    st = chan_merge(st, tile_stat<float, NS>(r, ks * 4));
+  }
+  const Stat cta = cta_merge<THREADS>(st, warp_part);
+  if (tid == 0) *bn_partial(p, u) = make_float4(cta.n, cta.mean, cta.m2, 0.f);
   pdl_trigger();
 }
 
@@ -80,19 +143,28 @@ template <int THREADS, int U, bool VEC>
 __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ float4 coef;
-  // reverse of the statistics pass's block order
+  // units in the reverse of memory order: the statistics pass read the last
+  // units most recently, so they are still in L2
   const int64_t nb = static_cast<int64_t>(gridDim.x);
   const int64_t lin = static_cast<int64_t>(gridDim.y) * nb - 1 -
                       (static_cast<int64_t>(blockIdx.y) * nb + blockIdx.x);
-  const int64_t c = lin / nb, b = lin - c * nb;
-  const int64_t n = b / p.chunks, k = b - n * p.chunks;
-  const int64_t off = (n * p.C + c) * p.S;
+  int64_t c, b, lo, hi, off;
+  if (p.N == 0) {
+    // an empty shard still merges the statistics and updates the running
+    // statistics (one CTA per channel) but has nothing to normalise
+    c = lin;
+    b = 0;
+    lo = hi = off = 0;
+  } else {
+    const BnUnit u = bn_unit(p, lin);
+    c = u.c;
+    b = u.n * p.chunks + u.k;
+    lo = u.lo;
+    hi = u.hi;
+    off = u.run * p.S;
+  }
   const float* xr = p.x + off;
   float* yr = p.y + off;
-  // (an empty shard -- N == 0 -- still merges the statistics and updates the
-  // running statistics, but has nothing to normalise)
-  const int64_t lo = k * p.chunk,
-                hi = p.N == 0 ? lo : ((lo + p.chunk < p.S) ? lo + p.chunk : p.S);
   pdl_wait();
 
   // channel statistics: the channel's partials (or the ranks' statistics)
@@ -263,24 +335,38 @@ static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <bool VEC>
-static cudaError_t bn_launch_t(const BnParams& p, cudaStream_t stream) {
+// The statistics pass: the split kernel in vector mode (unless
+// FNORM_BN_SPLIT=0 asks for the register-only kernel), the register-only
+// kernel otherwise.
+static cudaError_t bn_launch_stats(const BnParams& p, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
-  cudaError_t e = bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, VEC>, grid, stream, p);
-  if (e != cudaSuccess) return e;
-  return bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, VEC>, grid, stream, p);
+  if (p.vec && p.split) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBnThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(kBnThreads) * kBnSplitStaged * 16;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bn_stats_split_kernel<kBnThreads, kBnSplitRegs, kBnSplitStaged>, p);
+  }
+  return p.vec ? bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, true>, grid, stream, p)
+               : bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, false>, grid, stream, p);
 }
 
 cudaError_t bn_launch(const BnParams& p, cudaStream_t stream) {
-  return p.vec ? bn_launch_t<true>(p, stream) : bn_launch_t<false>(p, stream);
+  cudaError_t e = bn_launch_stats(p, stream);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
+  return p.vec ? bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
+               : bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
 }
 
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
-  cudaError_t e = p.vec ? bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, true>, grid,
-                                        stream, p)
-                        : bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, false>, grid,
-                                        stream, p);
+  cudaError_t e = bn_launch_stats(p, stream);
   if (e != cudaSuccess) return e;
   return bn_launch_one(&bn_merge_kernel<kBnThreads>, dim3(static_cast<unsigned>(p.C), 1, 1),
                        stream, p);

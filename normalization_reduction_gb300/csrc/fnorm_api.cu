@@ -631,6 +631,8 @@ void bn_fill(BnParams* p, const float* x, float* y, const float* gamma, const fl
   p->chunk = l.chunk;
   p->chunks = l.chunks;
   p->vec = aligned(x, 16) && (!y || aligned(y, 16)) && S % 4 == 0 && !env("FNORM_FORCE_SCALAR");
+  const char* split = env("FNORM_BN_SPLIT");
+  p->split = !(split && split[0] == '0');
   p->err = err;
 }
 

@@ -138,6 +138,7 @@ struct BnParams {
   int64_t stats_count;
   float4* local_out;    // [C] merged local statistics (local-stats call), else null
   bool vec;
+  bool split;           // statistics pass by the register + TMA-staged kernel (vector mode)
   unsigned* err;
 };
 
@@ -145,6 +146,10 @@ constexpr int kBnThreads = 256;
 constexpr int kBnUnroll = 4;        // apply pass: 16-byte loads per thread per tile
 constexpr int kBnStatsUnroll = 8;   // statistics pass
 constexpr int64_t kBnChunk = 16384;   // elements per CTA in the two streaming passes
+constexpr int kBnSplitRegs = 8;     // split statistics kernel: vectors per thread in registers
+constexpr int kBnSplitStaged = 8;   // ... and in TMA-staged shared memory (a whole kBnChunk unit)
+static_assert(kBnThreads * (kBnSplitRegs + kBnSplitStaged) * 4 >= kBnChunk,
+              "a unit must fit the split statistics kernel");
 
 cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);          // stats + apply
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream);  // stats + merge

@@ -68,6 +68,19 @@ def test_shapes(orc, shape):
     check(orc, x, g, b, what=str(shape))
 
 
+@pytest.mark.parametrize("shape", [(2, 1, 100000), (300, 3, 4), (5, 7, 36), (1, 200, 16384),
+                                   (3, 2, 49152), (9, 64, 15876), (4, 3, 8192), (4, 3, 8196),
+                                   (2, 5, 16380)])
+@pytest.mark.parametrize("split", ["1", "0"], ids=["split", "registers"])
+def test_statistics_kernels(orc, monkeypatch, shape, split):
+    """Both vector-mode statistics kernels (registers + TMA staging, registers
+    only): runs of many chunks, tiny runs of one vector, units that end in the
+    register part, in the staged part and exactly at the chunk size."""
+    monkeypatch.setenv("FNORM_BN_SPLIT", split)
+    x, g, b, _, _ = inputs.batchnorm(dev(), shape=shape, seed=11 + shape[-1])
+    check(orc, x, g, b, what=f"{shape} split={split}")
+
+
 def test_no_affine_no_running(orc):
     x, _, _, _, _ = inputs.batchnorm(dev(), shape=(4, 6, 300))
     check(orc, x, None, None, scale=1.0, with_running=False, what="plain")
