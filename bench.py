@@ -125,7 +125,7 @@ class Epilogue(Workload):
 
 class BatchNorm(Workload):
     name = "batchnorm2d_train_fp32_128x64x126x126"
-    kernel = "bn_apply_kernel"
+    kernel = "bn_stats_split_kernel+bn_apply_staged_kernel"
     launches = 2
 
     def __init__(self, dev):

@@ -227,6 +227,78 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
   }
 }
 
+// Apply pass in vector mode: the CTA's unit (<= kBnChunk values) is fetched
+// by one TMA bulk copy into shared memory, issued before the channel's
+// statistics are merged so that the merge overlaps the copy; then every
+// thread normalises staged vectors and streams them out. Same unit order,
+// statistics merge and side outputs as bn_apply_kernel.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnParams p) {
+  extern __shared__ __align__(16) uint4 stage[];   // kBnChunk / 4 vectors
+  __shared__ Stat warp_part[THREADS / 32];
+  __shared__ float4 coef;
+  __shared__ uint64_t bar;
+  const int tid = threadIdx.x;
+  const int64_t nb = static_cast<int64_t>(gridDim.x);
+  const int64_t lin = static_cast<int64_t>(gridDim.y) * nb - 1 -
+                      (static_cast<int64_t>(blockIdx.y) * nb + blockIdx.x);
+  const BnUnit u = bn_unit(p, lin);
+  const int64_t off = u.run * p.S + u.lo;
+  const int nvec = static_cast<int>((u.hi - u.lo) / 4);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (tid == 0 && nvec > 0) {
+    mbar_arrive_expect_tx(&bar, static_cast<unsigned>(nvec) * 16u);
+    tma_bulk_g2s(stage, p.x + off, static_cast<unsigned>(nvec) * 16u, &bar);
+  }
+  const float4* part = p.stats + u.c * p.stats_cstride;
+  Stat acc = stat_empty();
+  for (int64_t i = tid; i < p.stats_count; i += THREADS) {
+    const float4 v = part[i * p.stats_istride];
+    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
+  }
+  const Stat s = cta_merge<THREADS>(acc, warp_part);
+  if (tid == 0) {
+    const float var = s.m2 / s.n;
+    const float rstd = rsqrtf(var + p.eps);
+    const float g = p.gamma ? p.gamma[u.c] : 1.f;
+    const float bt = p.beta ? p.beta[u.c] : 0.f;
+    coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
+    if (u.n == 0 && u.k == 0) {
+      if (p.save_mean) p.save_mean[u.c] = s.mean;
+      if (p.save_rstd) p.save_rstd[u.c] = rstd;
+      if (p.running_mean && p.running_var) {
+        const double cnt = static_cast<double>(s.n);
+        const double mom = p.momentum;
+        const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
+        p.running_mean[u.c] = static_cast<float>((1.0 - mom) * p.running_mean[u.c] +
+                                                 mom * static_cast<double>(s.mean));
+        p.running_var[u.c] = static_cast<float>((1.0 - mom) * p.running_var[u.c] + mom * unbiased);
+      }
+    }
+  }
+  __syncthreads();
+  const float4 cf = coef;
+  if (nvec > 0) {
+    // a wait that gives up has flagged the error; it is retried once (bounded)
+    // so that the copy is not in flight when the CTA leaves
+    if (!mbar_wait_bounded(&bar, 0, p.err)) mbar_wait_bounded(&bar, 0, p.err);
+    float4* yv = reinterpret_cast<float4*>(p.y + off);
+#pragma unroll 4
+    for (int j = tid; j < nvec; j += THREADS) {
+      const uint4 r = stage[j];
+      float o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[q] = fmaf(Elem<float>::get(r, q) - cf.x, cf.y, cf.z);
+      __stcs(yv + j, make_float4(o[0], o[1], o[2], o[3]));
+    }
+  }
+}
+
 // Local statistics of a rank's shard: one CTA per channel merges the
 // channel's partials in a fixed order into local_out[c] = (n, mean, M2, 0).
 template <int THREADS>
@@ -357,12 +429,42 @@ static cudaError_t bn_launch_stats(const BnParams& p, cudaStream_t stream) {
                : bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, false>, grid, stream, p);
 }
 
+// The apply pass over N*chunks x C units (at least one CTA per channel).
+static cudaError_t bn_launch_apply_pass(const BnParams& p, cudaStream_t stream) {
+  const int64_t nb = p.N * p.chunks > 0 ? p.N * p.chunks : 1;
+  const dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(p.C), 1);
+  if (p.vec && p.split && p.N > 0) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const size_t smem = static_cast<size_t>(kBnChunk) * 4;
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(bn_apply_staged_kernel<kBnThreads>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBnThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bn_apply_staged_kernel<kBnThreads>, p);
+  }
+  return p.vec ? bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
+               : bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
+}
+
 cudaError_t bn_launch(const BnParams& p, cudaStream_t stream) {
   cudaError_t e = bn_launch_stats(p, stream);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
-  return p.vec ? bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
-               : bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
+  return bn_launch_apply_pass(p, stream);
 }
 
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {
@@ -389,10 +491,7 @@ cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream) {
 }
 
 cudaError_t bn_launch_apply(const BnParams& p, cudaStream_t stream) {
-  const int64_t nb = p.N * p.chunks > 0 ? p.N * p.chunks : 1;   // one CTA per channel if empty
-  const dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(p.C), 1);
-  return p.vec ? bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
-               : bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
+  return bn_launch_apply_pass(p, stream);
 }
 
 }  // namespace fnorm
