@@ -368,6 +368,45 @@ __global__ void __launch_bounds__(THREADS) bn_eval_kernel(const BnParams p) {
   pdl_trigger();
 }
 
+// Long runs in vector mode: one CTA per unit (<= kBnChunk values) fetched by
+// one TMA bulk copy into shared memory, so that the whole unit is in flight
+// while the channel's coefficients are formed.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 3) bn_eval_staged_kernel(const BnParams p) {
+  extern __shared__ __align__(16) uint4 stage[];   // kBnChunk / 4 vectors
+  __shared__ uint64_t bar;
+  const int tid = threadIdx.x;
+  const BnUnit u = bn_unit(p, static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x);
+  const int64_t off = u.run * p.S + u.lo;
+  const int nvec = static_cast<int>((u.hi - u.lo) / 4);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (tid == 0 && nvec > 0) {
+    mbar_arrive_expect_tx(&bar, static_cast<unsigned>(nvec) * 16u);
+    tma_bulk_g2s(stage, p.x + off, static_cast<unsigned>(nvec) * 16u, &bar);
+  }
+  const float4 cf = bn_eval_coef(p, u.c);
+  if (nvec > 0) {
+    // a wait that gives up has flagged the error; it is retried once (bounded)
+    // so that the copy is not in flight when the CTA leaves
+    if (!mbar_wait_bounded(&bar, 0, p.err)) mbar_wait_bounded(&bar, 0, p.err);
+    float4* yv = reinterpret_cast<float4*>(p.y + off);
+#pragma unroll 4
+    for (int j = tid; j < nvec; j += THREADS) {
+      const uint4 r = stage[j];
+      float o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o[q] = fmaf(Elem<float>::get(r, q) - cf.x, cf.y, cf.z);
+      yv[j] = make_float4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  pdl_trigger();
+}
+
 // Short runs (S < kBnEvalFlatBelow): a grid-stride loop over vectors (or
 // elements), each finding its channel from its index.
 template <int THREADS, bool VEC>
@@ -392,12 +431,14 @@ __global__ void __launch_bounds__(THREADS) bn_eval_flat_kernel(const BnParams p)
   pdl_trigger();
 }
 
-// Stream-ordered launch with programmatic dependent launch allowed.
+// Stream-ordered launch with programmatic dependent launch allowed; `smem`
+// bytes of dynamic shared memory.
 static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream_t stream,
-                                 const BnParams& p) {
+                                 const BnParams& p, size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kBnThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -407,24 +448,29 @@ static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// Allows `bytes` of dynamic shared memory for a staged kernel, once per device.
+static cudaError_t allow_smem(void (*kernel)(BnParams), size_t bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
+// One staged unit of kBnChunk fp32 values per CTA.
+constexpr size_t kBnStageBytes = static_cast<size_t>(kBnChunk) * 4;
+
 // The statistics pass: the split kernel in vector mode (unless
 // FNORM_BN_SPLIT=0 asks for the register-only kernel), the register-only
 // kernel otherwise.
 static cudaError_t bn_launch_stats(const BnParams& p, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
-  if (p.vec && p.split) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kBnThreads, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(kBnThreads) * kBnSplitStaged * 16;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bn_stats_split_kernel<kBnThreads, kBnSplitRegs, kBnSplitStaged>, p);
-  }
+  if (p.vec && p.split)
+    return bn_launch_one(&bn_stats_split_kernel<kBnThreads, kBnSplitRegs, kBnSplitStaged>, grid,
+                         stream, p, static_cast<size_t>(kBnThreads) * kBnSplitStaged * 16);
   return p.vec ? bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, true>, grid, stream, p)
                : bn_launch_one(&bn_stats_kernel<kBnThreads, kBnStatsUnroll, false>, grid, stream, p);
 }
@@ -434,28 +480,10 @@ static cudaError_t bn_launch_apply_pass(const BnParams& p, cudaStream_t stream) 
   const int64_t nb = p.N * p.chunks > 0 ? p.N * p.chunks : 1;
   const dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(p.C), 1);
   if (p.vec && p.split && p.N > 0) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    const size_t smem = static_cast<size_t>(kBnChunk) * 4;
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      const cudaError_t e = cudaFuncSetAttribute(bn_apply_staged_kernel<kBnThreads>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-      attr_set[dev] = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kBnThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bn_apply_staged_kernel<kBnThreads>, p);
+    static bool done[64] = {};
+    const cudaError_t e = allow_smem(&bn_apply_staged_kernel<kBnThreads>, kBnStageBytes, done);
+    if (e != cudaSuccess) return e;
+    return bn_launch_one(&bn_apply_staged_kernel<kBnThreads>, grid, stream, p, kBnStageBytes);
   }
   return p.vec ? bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
                : bn_launch_one(&bn_apply_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
@@ -477,6 +505,12 @@ cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {
 cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream) {
   if (p.S >= kBnEvalFlatBelow) {
     const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
+    if (p.vec && p.split) {
+      static bool done[64] = {};
+      const cudaError_t e = allow_smem(&bn_eval_staged_kernel<kBnThreads>, kBnStageBytes, done);
+      if (e != cudaSuccess) return e;
+      return bn_launch_one(&bn_eval_staged_kernel<kBnThreads>, grid, stream, p, kBnStageBytes);
+    }
     return p.vec ? bn_launch_one(&bn_eval_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
                  : bn_launch_one(&bn_eval_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
   }

@@ -147,9 +147,11 @@ EVAL_SHAPES = [(2, 3, 1), (4, 5, 7), (3, 4, 100), (2, 3, 1023), (2, 3, 1024), (5
 @pytest.mark.parametrize("shape", EVAL_SHAPES, ids=[f"{n}x{c}x{s}" for n, c, s in EVAL_SHAPES])
 @pytest.mark.parametrize("scalar", [False, True], ids=["vec", "scalar"])
 @pytest.mark.parametrize("affine", [True, False], ids=["affine", "plain"])
-def test_eval_shapes(orc, monkeypatch, shape, scalar, affine):
+@pytest.mark.parametrize("staged", ["1", "0"], ids=["staged", "registers"])
+def test_eval_shapes(orc, monkeypatch, shape, scalar, affine, staged):
     if scalar:
         monkeypatch.setenv("FNORM_FORCE_SCALAR", "1")
+    monkeypatch.setenv("FNORM_BN_SPLIT", staged)
     N, C, S = shape
     x, _, _ = inputs.per_channel_normal((N, C, S), 70_000 + S * C, dev())
     gamma, beta = params(C, 71 + S) if affine else (None, None)
