@@ -42,9 +42,14 @@ L2_BYTES = 126 * 1024 * 1024
 # DRAM bytes (read + write) per launch of each workload's dominant kernel from
 # one ncu capture (profiles/*.md); None until measured for the current kernel.
 NCU_TRAFFIC = {
-    # profiles/in_split_kernel__instancenorm_fp32_112x64x512x512.md: 1.073997 GB read +
-    # 1.019953 GB written for 1024 slices, scaled by 7 to the 7168-slice launch
-    "instancenorm2d_fp32_112x64x512x512": 14657650000,
+    # profiles/in_split_kernel__instancenorm_fp32_112x64x512x512.md: 1.073784 GB read +
+    # 1.016499 GB written for 1024 slices, scaled by 7 to the 7168-slice launch
+    "instancenorm2d_fp32_112x64x512x512": 14631981000,
+    # profiles/bn_eval_staged_kernel__batchnorm_eval_fp32_128x64x126x126.md (full size)
+    "batchnorm2d_eval_fp32_128x64x126x126": 984771328,
+    # profiles/bn_kernels__batchnorm_train_fp32_128x64x126x126.md: both launches of a step
+    # (caches flushed between them by ncu, so without the apply pass's L2 reuse)
+    "batchnorm2d_train_fp32_128x64x126x126": 1505755136,
 }
 
 
@@ -164,7 +169,7 @@ class InstanceNormAffine(InstanceNormLarge):
 class BatchNormEval(Workload):
     """Eval-mode BatchNorm2d(64) then x*2.0 on x[128,64,126,126]."""
     name = "batchnorm2d_eval_fp32_128x64x126x126"
-    kernel = "bn_eval_kernel"
+    kernel = "bn_eval_staged_kernel"
 
     def __init__(self, dev):
         self.x, self.g, self.b, self.rm, self.rv = inputs.batchnorm_eval(dev)
@@ -364,8 +369,43 @@ def time_graph(wl: Workload, steps: int, warmup: int, ws: int, sample_clocks=Fal
     return total_ms, [total_ms / steps] * steps, (sampler.summary() if sampler else None)
 
 
+def gpu_local_cpus(dev):
+    """CPUs of the NUMA node the GPU is attached to (sysfs), or None."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            if "-" in part:
+                a, b = part.split("-")
+                cpus.update(range(int(a), int(b) + 1))
+            elif part:
+                cpus.add(int(part))
+        return cpus & os.sched_getaffinity(0) or None
+    except Exception:
+        return None
+
+
 def e2e_instancenorm(wl: InstanceNormLarge, steps: int, chunk_slices: int = 224,
                      nstreams: int = 4):
+    """Binds the process to the GPU-local CPUs (when sysfs names them) while
+    the pinned buffers are allocated and used, then runs the timed loop."""
+    saved = os.sched_getaffinity(0)
+    local = gpu_local_cpus(wl.x.device)
+    if local:
+        os.sched_setaffinity(0, local)
+    try:
+        res = _e2e_instancenorm(wl, steps, chunk_slices, nstreams)
+    finally:
+        os.sched_setaffinity(0, saved)
+    res["host_cpus"] = f"{len(local)} GPU-local" if local else "unbound"
+    return res
+
+
+def _e2e_instancenorm(wl: InstanceNormLarge, steps: int, chunk_slices: int = 224,
+                      nstreams: int = 4):
     """Same metric through the C ABI with the input and output in pinned HOST
     memory: every step copies x host->device, normalises, copies y back.
     Chunks of slices go round-robin over several streams so the copies in both
