@@ -7,22 +7,27 @@
 //
 // A channel's values are N runs of S contiguous elements, C*S apart. A channel
 // of the page's tensor (128 x 126 x 126 fp32 = 8.1 MB) is far larger than any
-// on-chip store, so x is read twice, in two launches:
-//   1. bn_stats_kernel -- one CTA per (run, chunk of <= 16384 elements):
-//                         128-bit loads (8 per thread in flight), exact
-//                         two-pass per register tile, Chan merges -> one
-//                         partial (n, mean, M2) per CTA in the caller's
-//                         workspace;
-//   2. bn_apply_kernel -- one CTA per (run, chunk), visiting them in the
-//                         reverse of the statistics pass so the last ~100 MB
-//                         it read are still in L2. Each CTA first merges its
-//                         channel's partials in a fixed tree (every CTA of the
-//                         channel obtains bit-identical statistics), forms
-//                         y = (x - mean)*A + B with A = scale*gamma*rstd and
-//                         B = scale*beta, and stores with evict-first hints so
-//                         the output does not push the reusable input out of
-//                         L2. The CTA of run 0, chunk 0 also writes the saved
-//                         statistics and updates the running statistics.
+// on-chip store, so x is read twice, in two launches over "units" (one run,
+// or a chunk of <= 16384 values of a longer run), in memory order:
+//   1. statistics -- one CTA per unit; in vector mode the whole unit is in
+//                    flight at once (bn_stats_split_kernel: 128-bit register
+//                    loads plus one TMA bulk copy into shared memory), exact
+//                    two-pass per thread, Chan merges -> one partial
+//                    (n, mean, M2) per unit in the caller's workspace;
+//   2. apply      -- one CTA per unit, in the reverse of memory order so the
+//                    last ~100 MB the statistics pass read are still in L2
+//                    (bn_apply_staged_kernel: the unit's TMA copy is issued
+//                    before the channel's partials are merged in a fixed tree,
+//                    so every CTA of a channel obtains bit-identical
+//                    statistics); y = (x - mean)*A + B with A = scale*gamma*rstd,
+//                    B = scale*beta; evict-first stores keep the reusable
+//                    input in L2. The CTA of (n = 0, chunk 0) writes the saved
+//                    statistics and updates the running statistics.
+// Eval mode (running statistics) is one elementwise pass (bn_eval_*_kernel).
+// Element-wise (unaligned or S % 4 != 0) inputs take register-only kernels
+// with the same unit order and results.
+#include <atomic>
+
 #include "fnorm_device.cuh"
 #include "fnorm_internal.h"
 #include "in_kernels.cuh"
@@ -449,14 +454,16 @@ static cudaError_t bn_launch_one(void (*kernel)(BnParams), dim3 grid, cudaStream
 }
 
 // Allows `bytes` of dynamic shared memory for a staged kernel, once per device.
-static cudaError_t allow_smem(void (*kernel)(BnParams), size_t bytes, bool (&done)[64]) {
+// (Setting the attribute is idempotent, so racing host threads are harmless.)
+static cudaError_t allow_smem(void (*kernel)(BnParams), size_t bytes,
+                              std::atomic<bool> (&done)[64]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(bytes));
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
@@ -480,7 +487,7 @@ static cudaError_t bn_launch_apply_pass(const BnParams& p, cudaStream_t stream) 
   const int64_t nb = p.N * p.chunks > 0 ? p.N * p.chunks : 1;
   const dim3 grid(static_cast<unsigned>(nb), static_cast<unsigned>(p.C), 1);
   if (p.vec && p.split && p.N > 0) {
-    static bool done[64] = {};
+    static std::atomic<bool> done[64];
     const cudaError_t e = allow_smem(&bn_apply_staged_kernel<kBnThreads>, kBnStageBytes, done);
     if (e != cudaSuccess) return e;
     return bn_launch_one(&bn_apply_staged_kernel<kBnThreads>, grid, stream, p, kBnStageBytes);
@@ -506,7 +513,7 @@ cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream) {
   if (p.S >= kBnEvalFlatBelow) {
     const dim3 grid(static_cast<unsigned>(p.N * p.chunks), static_cast<unsigned>(p.C), 1);
     if (p.vec && p.split) {
-      static bool done[64] = {};
+      static std::atomic<bool> done[64];
       const cudaError_t e = allow_smem(&bn_eval_staged_kernel<kBnThreads>, kBnStageBytes, done);
       if (e != cudaSuccess) return e;
       return bn_launch_one(&bn_eval_staged_kernel<kBnThreads>, grid, stream, p, kBnStageBytes);

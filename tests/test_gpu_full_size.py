@@ -12,6 +12,8 @@ times (the library's default plan):
   sampled slices per S against the oracle.
 * Affine InstanceNorm fp32 x[112,64,512,512]: 16 sampled slices.
 * Eval BatchNorm fp32 x[128,64,126,126]: five sampled samples n.
+* InstanceNorm fp32 x[132,64,512,512] (more than 2^31 elements): slices around the 32-bit
+  element and byte boundaries.
 """
 import numpy as np
 import pytest
@@ -148,3 +150,23 @@ def test_batchnorm_eval_full_size(orc):
                              rv.cpu().numpy(), EPS)
     assert_close(y.index_select(0, pick).cpu().numpy().reshape(5, C, S), ref, torch.float32,
                  "eval BN")
+
+
+def test_instancenorm_beyond_2e31_elements(orc):
+    """x[132,64,512,512] fp32 = 2.21e9 elements (> 2^31; 8.9 GB each way): slices around the
+    element offsets 2^30 (byte offset 2^32) and 2^31, and the last slices, against the oracle."""
+    shape = (132, 64, 512, 512)
+    N, C, H, W = shape
+    NC, S = N * C, H * W
+    assert NC * S > 2 ** 31
+    x = inputs.instancenorm_large(dev(), shape=shape, seed=1102)
+    y = torch.empty_like(x)
+    fn.fnorm_instancenorm(x, y, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None)
+    torch.cuda.synchronize()
+    idx = np.array([0, 4095, 4096, 4097, 8191, 8192, 8193, NC - 2, NC - 1])
+    ti = torch.from_numpy(idx).to(dev())
+    xs = x.view(NC, S).index_select(0, ti).cpu().numpy()
+    ref, _, _ = orc.instancenorm(xs, EPS)
+    assert_close(y.view(NC, S).index_select(0, ti).cpu().numpy(), ref, torch.float32, "> 2^31")
+    del x, y
+    torch.cuda.empty_cache()
