@@ -49,8 +49,9 @@ size_t epi_range_smem(int64_t C, int64_t per, int cluster) {
          2 * static_cast<size_t>(C) * cluster * 16;
 }
 
-size_t epi_range_l2_smem(int64_t C, int cluster) {
-  return static_cast<size_t>(C) * 16 + 2 * static_cast<size_t>(C) * cluster * 16;
+size_t epi_range_l2_smem(int64_t C, int cluster, int keep) {
+  return static_cast<size_t>(C) * 16 + 2 * static_cast<size_t>(C) * cluster * 16 +
+         static_cast<size_t>(C) * keep * 16;
 }
 
 size_t epi_ring_smem(int64_t C, int ring_t, int cluster) {
@@ -278,7 +279,9 @@ __device__ __forceinline__ void epi_take(const uint4& u, const float4& k, int c,
   }
 }
 
-template <int THREADS, bool WANT_ARG>
+// KEEP >= 0 fixes the kept vectors per channel at compile time (the common
+// full-size case); KEEP < 0 takes p.keep.
+template <int THREADS, bool WANT_ARG, int KEEP>
 __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParams p) {
   extern __shared__ __align__(16) float4 dyn[];
   __shared__ __align__(8) uint64_t xbar[2];
@@ -294,6 +297,10 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float4* coef = dyn;          // [C]
   float4* slots = dyn + C;     // [2][C][csize]
+  // [C][KS]: the first KS position vectors of each channel of the range, kept
+  // from the statistics pass for the output pass (fewer L2 re-reads)
+  uint4* keep = reinterpret_cast<uint4*>(slots + 2 * C * csize);
+  const int KS = KEEP >= 0 ? KEEP : p.keep;
   const int64_t nv4 = S / 4;
   const int64_t v0 = per * crank;
   const int vr = static_cast<int>(v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0);
@@ -323,6 +330,11 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
         uint4 r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) r[u] = ld_v4(xc + t + u * 32);
+        if (t == 0) {
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (u * 32 + lane < KS) keep[c * KS + u * 32 + lane] = r[u];
+        }
         acc = chan_merge(acc, tile_stat_full<float, U>(r));
       }
       if (t < vr) {                              // ragged tail
@@ -333,6 +345,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
           const bool v = t + u * 32 + lane < vr;
           r[u] = v ? ld_v4(xc + t + u * 32) : make_uint4(0, 0, 0, 0);
           nvalid += v ? 4 : 0;
+          if (t == 0 && v && u * 32 + lane < KS) keep[c * KS + u * 32 + lane] = r[u];
         }
         acc = chan_merge(acc, tile_stat<float, U>(r, nvalid));
       }
@@ -358,7 +371,26 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       if (lane == 0) coef[c] = epi_out_coef(s, __ldg(p.m + c), p.eps, p.lo, p.hi);
     }
     __syncthreads();
-    for (int v = tid; v < vr; v += THREADS) {
+    const int vk = vr < KS ? vr : KS;
+    for (int v = tid; v < vk; v += THREADS) {   // positions kept on chip
+      float best[4];
+      int arg[4] = {0, 0, 0, 0};
+      {
+        const uint4 u = keep[v];
+        const float4 k = coef[0];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) best[j] = epi_zc(Elem<float>::get(u, j), k);
+      }
+      for (int c = 1; c < C; ++c) epi_take<WANT_ARG>(keep[c * KS + v], coef[c], c, best, arg);
+      const int64_t pos = (v0 + v) * 4;
+      __stcs(reinterpret_cast<float4*>(p.y + n * S + pos), make_float4(best[0], best[1], best[2], best[3]));
+      if (WANT_ARG) {
+        longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pos);
+        __stcs(ao, make_longlong2(arg[0], arg[1]));
+        __stcs(ao + 1, make_longlong2(arg[2], arg[3]));
+      }
+    }
+    for (int v = vk + tid; v < vr; v += THREADS) {
       const uint4* xv = xn + v;
       float best[4];
       int arg[4] = {0, 0, 0, 0};
@@ -700,8 +732,11 @@ static EpiKernelFn epi_kernel(const EpiPlan& plan) {
       return plan.want_arg ? &epi_range_kernel<kEpiThreads, true>
                            : &epi_range_kernel<kEpiThreads, false>;
     case EpiPath::kRangeL2:
-      return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true>
-                           : &epi_range_l2_kernel<kEpiThreads, false>;
+      if (plan.keep == kEpiKeepMax)
+        return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, kEpiKeepMax>
+                             : &epi_range_l2_kernel<kEpiThreads, false, kEpiKeepMax>;
+      return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, -1>
+                           : &epi_range_l2_kernel<kEpiThreads, false, -1>;
     case EpiPath::kRing:
       return plan.want_arg ? &epi_ring_kernel<true> : &epi_ring_kernel<false>;
     case EpiPath::kStream: return &epi_stream_kernel<kEpiThreads>;

@@ -381,8 +381,13 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
     const int64_t nv4 = S / 4;
     const int64_t per = (nv4 + cl - 1) / cl;
     const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
+    int keep = static_cast<int>(kEpiKeepBudget / (C * 16));
+    if (keep > kEpiKeepMax) keep = kEpiKeepMax;
+    if (keep > per) keep = static_cast<int>(per);
+    if (const char* k = env("FNORM_EPI_KEEP")) keep = std::atoi(k) < keep ? std::atoi(k) : keep;
+    if (keep < 0) keep = 0;
     EpiPlan cand{EpiPath::kRangeL2, kEpiThreads, cl_eff, per, argmax != nullptr, 0,
-                 epi_range_l2_smem(C, cl_eff), 0};
+                 epi_range_l2_smem(C, cl_eff, keep), 0, keep};
     if (cl >= 1 && cl <= kMaxCluster && epi_capacity(cand) > 0) {
       plan = cand;
       have = true;
@@ -401,10 +406,10 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   plan.grid = static_cast<int>(clusters * plan.cluster);
   if (env("FNORM_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d per=%lld ring_t=%d smem=%zu "
-                 "grid=%d capacity=%d\n",
+                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d per=%lld ring_t=%d keep=%d "
+                 "smem=%zu grid=%d capacity=%d\n",
                  static_cast<int>(plan.path), plan.cluster, static_cast<long long>(plan.per),
-                 plan.ring_t, plan.smem, plan.grid, cap);
+                 plan.ring_t, plan.keep, plan.smem, plan.grid, cap);
   *out = plan;
   return FNORM_OK;
 }
@@ -567,6 +572,7 @@ fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* 
   p.per = plan.per;
   p.debug_timeout = env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0;
   p.ring_t = plan.ring_t;
+  p.keep = plan.keep;
   p.err = err;
   return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }

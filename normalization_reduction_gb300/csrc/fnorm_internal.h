@@ -81,6 +81,7 @@ struct EpiParams {
   int64_t per;         // position vectors (of 4) per CTA (range path)
   int debug_timeout;   // test hook: wait on an mbarrier nobody completes
   int ring_t;          // position vectors per ring stage (ring path)
+  int keep;            // position vectors per channel kept in shared memory between passes (L2 path)
   unsigned* err;
 };
 
@@ -97,6 +98,7 @@ struct EpiPlan {
   int ring_t;
   size_t smem;   // dynamic shared memory bytes
   int grid;      // CTAs (multiple of cluster)
+  int keep;      // L2 path: position vectors per channel kept on chip
 };
 
 constexpr int kEpiThreads = 256;
@@ -106,7 +108,11 @@ constexpr int kEpiMaxChannels = 8192;
 cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t stream);
 int epi_max_active_clusters(const EpiPlan& plan);
 size_t epi_range_smem(int64_t C, int64_t per, int cluster);
-size_t epi_range_l2_smem(int64_t C, int cluster);
+size_t epi_range_l2_smem(int64_t C, int cluster, int keep);
+// L2 path: the leading position vectors of each channel of a CTA's range that
+// stay in shared memory from the statistics pass to the output pass.
+constexpr int kEpiKeepMax = 160;
+constexpr int kEpiKeepBudget = 40960;   // bytes (keeps the CTA under 48 KB of dynamic smem)
 size_t epi_ring_smem(int64_t C, int ring_t, int cluster);
 size_t epi_stream_smem(int64_t C, int cluster);
 

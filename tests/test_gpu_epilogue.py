@@ -72,6 +72,20 @@ def test_variant_shapes(orc, monkeypatch, shape, variant):
     check(orc, x, m, what=f"{variant} {shape}")
 
 
+@pytest.mark.parametrize("keep", ["0", "1", "37", "160"])
+@pytest.mark.parametrize("shape", [(4, 16, 14, 30, 30), (3, 5, 1000), (2, 1, 4096), (3, 40, 1000),
+                                   (2, 9, 4), (2, 3, 2052)])
+@pytest.mark.parametrize("cl", ["2", "4"])
+def test_l2_keep_sizes(orc, monkeypatch, shape, keep, cl):
+    """The L2-form kernel with 0 .. 160 position vectors per channel kept in
+    shared memory between its passes (ranges shorter and longer than the kept
+    part, kept parts that end inside a tile)."""
+    monkeypatch.setenv("FNORM_EPI_KEEP", keep)
+    monkeypatch.setenv("FNORM_EPI_CLUSTER", cl)
+    x, m = inputs.epilogue(dev(), shape=shape, seed=777 + shape[1])
+    check(orc, x, m, what=f"keep {keep} {shape} cl {cl}")
+
+
 @pytest.mark.parametrize("cl", [1, 2, 4, 8])
 def test_ring_cluster_sizes(orc, monkeypatch, cl):
     monkeypatch.setenv("FNORM_EPI_RING", "1")
