@@ -189,9 +189,10 @@ class Sweep(Workload):
     kernel = "in_*_kernel"
     dtype = "bf16"
 
-    def __init__(self, dev, S):
-        self.name = f"instancenorm_bf16_sweep_S{S}"
-        self.x = inputs.instancenorm_sweep(S, dev)
+    def __init__(self, dev, S, total=inputs.SWEEP_TOTAL):
+        self.name = f"instancenorm_bf16_sweep_S{S}" + ("" if total == inputs.SWEEP_TOTAL
+                                                       else f"_total{total}")
+        self.x = inputs.instancenorm_sweep(S, dev, total=total)
         self.y = torch.empty_like(self.x)
         self.N, self.C, self.S = self.x.shape
 
@@ -289,7 +290,9 @@ def make_workload(args, dev) -> Workload:
     if args.workload == "bn_eval":
         return BatchNormEval(dev)
     if args.workload.startswith("sweep:"):
-        return Sweep(dev, int(args.workload.split(":")[1]))
+        parts = args.workload.split(":")
+        total = int(parts[2]) if len(parts) > 2 else inputs.SWEEP_TOTAL
+        return Sweep(dev, int(parts[1]), total)
     raise SystemExit(f"unknown workload {args.workload}")
 
 
@@ -578,8 +581,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip e2e, cpu baseline and the other workloads")
     ap.add_argument("--workload", default="in_large",
-                    help="in_large | in_affine | epilogue | batchnorm | bn_eval | sweep:S "
-                         "(S a power of 4, 256..4^10)")
+                    help="in_large | in_affine | epilogue | batchnorm | bn_eval | sweep:S[:TOTAL] "
+                         "(S a power of 4, 256..4^10; TOTAL elements, default 2^30)")
     ap.add_argument("--shape", default=None,
                     help="N,C,H,W for in_large (e.g. a smaller case for ncu)")
     args = ap.parse_args()
