@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnPara
   extern __shared__ __align__(16) uint4 stage[];   // (THREADS * NS) vectors
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ uint64_t bar;
+  __shared__ uint64_t dbg_bar;
   const int tid = threadIdx.x;
   const BnUnit u = bn_unit(p, static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x);
   const uint4* xv = reinterpret_cast<const uint4*>(p.x + u.run * p.S + u.lo);
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnPara
   const int svec = nvec > RV ? nvec - RV : 0;
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&dbg_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -142,6 +144,10 @@ __global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnPara
   const Stat cta = cta_merge<THREADS>(st, warp_part);
   if (tid == 0) *bn_partial(p, u) = make_float4(cta.n, cta.mean, cta.m2, 0.f);
   pdl_trigger();
+  // Test hook: one CTA waits on a barrier nothing completes; the wait must
+  // expire, record the timeout in the error word and return.
+  if (p.debug_timeout && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
+    mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
 template <int THREADS, int U, bool VEC>
@@ -243,6 +249,7 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ float4 coef;
   __shared__ uint64_t bar;
+  __shared__ uint64_t dbg_bar;
   const int tid = threadIdx.x;
   const int64_t nb = static_cast<int64_t>(gridDim.x);
   const int64_t lin = static_cast<int64_t>(gridDim.y) * nb - 1 -
@@ -252,6 +259,7 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
   const int nvec = static_cast<int>((u.hi - u.lo) / 4);
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&dbg_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -302,6 +310,10 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
       __stcs(yv + j, make_float4(o[0], o[1], o[2], o[3]));
     }
   }
+  // Test hook: one CTA waits on a barrier nothing completes; the wait must
+  // expire, record the timeout in the error word and return.
+  if (p.debug_timeout && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
+    mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
 // Local statistics of a rank's shard: one CTA per channel merges the
@@ -380,12 +392,14 @@ template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 3) bn_eval_staged_kernel(const BnParams p) {
   extern __shared__ __align__(16) uint4 stage[];   // kBnChunk / 4 vectors
   __shared__ uint64_t bar;
+  __shared__ uint64_t dbg_bar;
   const int tid = threadIdx.x;
   const BnUnit u = bn_unit(p, static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x);
   const int64_t off = u.run * p.S + u.lo;
   const int nvec = static_cast<int>((u.hi - u.lo) / 4);
   if (tid == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&dbg_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -410,6 +424,10 @@ __global__ void __launch_bounds__(THREADS, 3) bn_eval_staged_kernel(const BnPara
     }
   }
   pdl_trigger();
+  // Test hook: one CTA waits on a barrier nothing completes; the wait must
+  // expire, record the timeout in the error word and return.
+  if (p.debug_timeout && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
+    mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
 // Short runs (S < kBnEvalFlatBelow): a grid-stride loop over vectors (or

@@ -521,7 +521,8 @@ fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const float* gamm
   if (st != FNORM_OK) return st;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
-  const InParams p{x, y, NC, S, eps, mean_out, rstd_out, err, gamma, beta, C};
+  const InParams p{x,    y,     NC,   S, eps, mean_out, rstd_out, err, gamma, beta, C,
+                   env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0};
   return cuda_status(in_launch_dispatch(tin, tout, p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -639,6 +640,7 @@ void bn_fill(BnParams* p, const float* x, float* y, const float* gamma, const fl
   p->vec = aligned(x, 16) && (!y || aligned(y, 16)) && S % 4 == 0 && !env("FNORM_FORCE_SCALAR");
   const char* split = env("FNORM_BN_SPLIT");
   p->split = !(split && split[0] == '0');
+  p->debug_timeout = env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0;
   p->err = err;
 }
 

@@ -78,6 +78,7 @@ struct Elem<float> {
     const unsigned w = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
     return __uint_as_float(w);
   }
+  __device__ static __forceinline__ float get_opaque(const uint4& v, int j) { return get(v, j); }
   __device__ static __forceinline__ void set(uint4& v, int j, float f) {
     const unsigned w = __float_as_uint(f);
     if (j == 0) v.x = w; else if (j == 1) v.y = w; else if (j == 2) v.z = w; else v.w = w;
@@ -92,6 +93,19 @@ struct Elem<__nv_bfloat16> {
   __device__ static __forceinline__ float get(const uint4& v, int j) {
     const unsigned w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
     return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+  // The same widening as an opaque one-instruction asm that the compiler
+  // re-does at every use instead of keeping 8 widened values per slot live
+  // across the passes (which doubles a slot's registers and spills in the
+  // kernels that hold 8 slots per thread).
+  __device__ static __forceinline__ float get_opaque(const uint4& v, int j) {
+    const unsigned w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
+    unsigned r;
+    if (j & 1)
+      asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(r) : "r"(w));
+    else
+      asm volatile("shl.b32 %0, %1, 16;" : "=r"(r) : "r"(w));
+    return __uint_as_float(r);
   }
   __device__ static __forceinline__ void set(uint4& v, int j, float f) {
     // f is a bf16 value widened to fp32 (exact), so its low 16 bits are zero

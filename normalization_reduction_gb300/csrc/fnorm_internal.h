@@ -24,6 +24,7 @@ struct InParams {
   const float* gamma;   // [C] per-channel scale (nullptr: 1)
   const float* beta;    // [C] per-channel shift (nullptr: 0)
   int64_t C;            // channels: slice q belongs to channel q % C
+  int debug_timeout;    // test hook (split kernel): wait on an mbarrier nobody completes
 };
 
 enum class InPath : int {
@@ -145,6 +146,7 @@ struct BnParams {
   float4* local_out;    // [C] merged local statistics (local-stats call), else null
   bool vec;
   bool split;           // statistics pass by the register + TMA-staged kernel (vector mode)
+  int debug_timeout;    // test hook (staged kernels): wait on an mbarrier nobody completes
   unsigned* err;
 };
 

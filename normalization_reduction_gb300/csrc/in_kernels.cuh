@@ -35,16 +35,23 @@ namespace fnorm {
 
 // Exact two-pass statistics of the first `nvalid` values of a thread's slots
 // (values in (k, j) order: slot k, element j). Invalid values are ignored.
-template <class Tin, int NV>
+// Widened value j of a 16-byte slot; OPAQUE re-does the widening at every use
+// (see Elem<__nv_bfloat16>::get_opaque).
+template <class E, bool OPAQUE>
+__device__ __forceinline__ float widen(const uint4& v, int j) {
+  return OPAQUE ? E::get_opaque(v, j) : E::get(v, j);
+}
+
+template <class Tin, int NV, bool OPAQUE = false>
 __device__ __forceinline__ Stat tile_stat_full(const uint4 (&r)[NV]) {
   using E = Elem<Tin>;
   constexpr int W = E::W;
-  const float x0 = E::get(r[0], 0);
+  const float x0 = widen<E, OPAQUE>(r[0], 0);
   float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < NV; ++k)
 #pragma unroll
-    for (int j = 0; j < W; ++j) s[j & 3] += E::get(r[k], j) - x0;
+    for (int j = 0; j < W; ++j) s[j & 3] += widen<E, OPAQUE>(r[k], j) - x0;
   constexpr float n = static_cast<float>(NV * W);
   const float mean = x0 + ((s[0] + s[1]) + (s[2] + s[3])) * (1.0f / n);
   float q[4] = {0.f, 0.f, 0.f, 0.f};
@@ -52,25 +59,25 @@ __device__ __forceinline__ Stat tile_stat_full(const uint4 (&r)[NV]) {
   for (int k = 0; k < NV; ++k)
 #pragma unroll
     for (int j = 0; j < W; ++j) {
-      const float d = E::get(r[k], j) - mean;
+      const float d = widen<E, OPAQUE>(r[k], j) - mean;
       q[j & 3] = fmaf(d, d, q[j & 3]);
     }
   return Stat{n, mean, (q[0] + q[1]) + (q[2] + q[3])};
 }
 
-template <class Tin, int NV, bool FAST = true>
+template <class Tin, int NV, bool FAST = true, bool OPAQUE = false>
 __device__ __forceinline__ Stat tile_stat(const uint4 (&r)[NV], int nvalid) {
   using E = Elem<Tin>;
   constexpr int W = E::W;
-  if (FAST && nvalid == NV * W) return tile_stat_full<Tin, NV>(r);   // no per-value predicates
+  if (FAST && nvalid == NV * W) return tile_stat_full<Tin, NV, OPAQUE>(r);   // no per-value predicates
   if (nvalid <= 0) return stat_empty();
-  const float x0 = E::get(r[0], 0);
+  const float x0 = widen<E, OPAQUE>(r[0], 0);
   float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < NV; ++k)
 #pragma unroll
     for (int j = 0; j < W; ++j) {
-      const float d = E::get(r[k], j) - x0;
+      const float d = widen<E, OPAQUE>(r[k], j) - x0;
       s[j & 3] += (k * W + j < nvalid) ? d : 0.f;
     }
   const float n = static_cast<float>(nvalid);
@@ -80,7 +87,7 @@ __device__ __forceinline__ Stat tile_stat(const uint4 (&r)[NV], int nvalid) {
   for (int k = 0; k < NV; ++k)
 #pragma unroll
     for (int j = 0; j < W; ++j) {
-      const float d = E::get(r[k], j) - mean;
+      const float d = widen<E, OPAQUE>(r[k], j) - mean;
       q[j & 3] += (k * W + j < nvalid) ? d * d : 0.f;
     }
   return Stat{n, mean, (q[0] + q[1]) + (q[2] + q[3])};
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
 
     // (no full-tile fast path here: a second unrolled copy of the two-pass would
     // push the 64-register budget of 8 bf16 slots per thread into spills)
-    const Stat cta = cta_merge<THREADS>(tile_stat<Tin, NV, false>(r, nvalid), warp_part);
+    const Stat cta = cta_merge<THREADS>(tile_stat<Tin, NV, false, true>(r, nvalid), warp_part);
     const float2 mr = cluster_finalize<THREADS>(cta, cta_part, &fin, csize, it, p.eps);
     if (crank == 0 && tid == 0) {
       if (p.mean_out) p.mean_out[q] = mr.x;
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
         if (k * W < nvalid) {
           float o[W];
 #pragma unroll
-          for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y);
+          for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(r[k], j) - mr.x, ab.x, ab.y);
           VecStore<Tout, W>::run(yv + static_cast<int64_t>(k) * THREADS * W, o);
         }
       }
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(THREADS, resident_min_blocks(THREADS, NV))
         for (int j = 0; j < W; ++j)
           if (k * W + j < nvalid)
             Elem<Tout>::store1(ys + first + static_cast<int64_t>(k * W + j) * THREADS,
-                               fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y));
+                               fmaf(E::get_opaque(r[k], j) - mr.x, ab.x, ab.y));
     }
   }
   pdl_trigger();
@@ -498,6 +505,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
   __shared__ float2 fin;
   __shared__ __align__(8) uint64_t tma_bar;
   __shared__ __align__(8) uint64_t xbar[2];
+  __shared__ __align__(8) uint64_t dbg_bar;
 
   const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
   const unsigned cid = cluster_id_x(), ncl = ncluster_x();
@@ -521,6 +529,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     mbar_init(&tma_bar, 1);
     mbar_init(&xbar[0], 1);
     mbar_init(&xbar[1], 1);
+    mbar_init(&dbg_bar, 1);
     fence_mbar_init();
   }
   if (csize > 1) cluster_sync();   // peers' barriers exist before anyone signals them
@@ -550,21 +559,21 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     // exact two-pass over this thread's values, shifted by its first value
     Stat st = stat_empty();
     if (nvalid > 0) {
-      const float x0 = E::get(ns_valid > 0 ? stage[tid] : r[0], 0);
+      const float x0 = E::get_opaque(ns_valid > 0 ? stage[tid] : r[0], 0);
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < NS; ++k) {
         if (k < ns_valid) {
           const uint4 v = stage[k * THREADS + tid];
 #pragma unroll
-          for (int j = 0; j < W; ++j) s4[j & 3] += E::get(v, j) - x0;
+          for (int j = 0; j < W; ++j) s4[j & 3] += E::get_opaque(v, j) - x0;
         }
       }
 #pragma unroll
       for (int k = 0; k < NR; ++k) {
         if (k < nr_valid) {
 #pragma unroll
-          for (int j = 0; j < W; ++j) s4[j & 3] += E::get(r[k], j) - x0;
+          for (int j = 0; j < W; ++j) s4[j & 3] += E::get_opaque(r[k], j) - x0;
         }
       }
       const float n = static_cast<float>(nvalid);
@@ -576,7 +585,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
           const uint4 v = stage[k * THREADS + tid];
 #pragma unroll
           for (int j = 0; j < W; ++j) {
-            const float d = E::get(v, j) - mean;
+            const float d = E::get_opaque(v, j) - mean;
             q4[j & 3] = fmaf(d, d, q4[j & 3]);
           }
         }
@@ -586,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
         if (k < nr_valid) {
 #pragma unroll
           for (int j = 0; j < W; ++j) {
-            const float d = E::get(r[k], j) - mean;
+            const float d = E::get_opaque(r[k], j) - mean;
             q4[j & 3] = fmaf(d, d, q4[j & 3]);
           }
         }
@@ -609,7 +618,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
         const uint4 v = stage[k * THREADS + tid];
         float o[W];
 #pragma unroll
-        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(v, j) - mr.x, ab.x, ab.y);
+        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(v, j) - mr.x, ab.x, ab.y);
         VecStore<Tout, W>::run(yq + (base + int64_t(k) * THREADS + tid) * W, o);
       }
     }
@@ -627,7 +636,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
       if (k < nr_valid) {
         float o[W];
 #pragma unroll
-        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get(r[k], j) - mr.x, ab.x, ab.y);
+        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(r[k], j) - mr.x, ab.x, ab.y);
         VecStore<Tout, W>::run(yq + (rbase + int64_t(k) * THREADS) * W, o);
       }
     }
@@ -640,6 +649,10 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
   pdl_trigger();
   if (csize > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
   if (failed && sbytes > 0) mbar_wait_bounded(&tma_bar, tparity, p.err);
+  // Test hook, after the last cluster barrier so no peer waits on this CTA: a
+  // wait on a barrier nothing completes must expire, record the timeout in the
+  // error word and return.
+  if (p.debug_timeout && cid == 0 && crank == 0 && tid == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
 // ---------------------------------------------------------------------------

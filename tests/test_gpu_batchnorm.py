@@ -143,3 +143,29 @@ def test_deterministic():
     y1, m1, r1 = run_bn(x, g, b, None, None)
     y2, m2, r2 = run_bn(x, g, b, None, None)
     assert torch.equal(y1, y2) and torch.equal(m1, m2) and torch.equal(r1, r2)
+
+
+@pytest.mark.parametrize("mode", ["train", "eval"])
+def test_bounded_wait_timeout(orc, monkeypatch, mode):
+    """The test hook makes one CTA of each staged BatchNorm kernel wait on an
+    mbarrier nothing completes: the waits expire, the error word reports
+    FNORM_ERR_TIMEOUT (read and cleared) and the results are still correct."""
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    x, g, b, _, _ = inputs.batchnorm(dev(), shape=(6, 5, 3000))
+    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    if mode == "train":
+        y, _, _ = run_bn(x, g, b, None, None)
+        ref, _, _, _, _ = orc.batchnorm_train(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(),
+                                              2.0, None, None, MOM, EPS)
+    else:
+        rm = torch.linspace(-0.1, 0.1, 5, device=dev())
+        rv = torch.linspace(0.5, 1.5, 5, device=dev())
+        y = torch.empty_like(x)
+        fn.fnorm_batchnorm_eval(x, y, g, b, 2.0, rm, rv, EPS, 6, 5, 3000)
+        torch.cuda.synchronize()
+        ref = orc.batchnorm_eval(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(), 2.0,
+                                 rm.cpu().numpy(), rv.cpu().numpy(), EPS)
+    assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    assert_close(y.cpu().numpy(), ref, torch.float32, f"{mode} after timeout")

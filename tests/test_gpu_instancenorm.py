@@ -203,3 +203,21 @@ def test_mixed_scale_slices(orc):
     y, _, _ = run_in(x)
     ref, _, _ = oracle_in(orc, x)
     assert_close(to_f64(y), ref, torch.float32, "mixed scales")
+
+
+def test_bounded_wait_timeout(orc, monkeypatch):
+    """The test hook makes one CTA of the split kernel wait, after its last
+    cluster barrier, on an mbarrier nothing completes: the wait expires after
+    its limit, the error word reports FNORM_ERR_TIMEOUT (read and cleared), the
+    context stays usable and the results are correct."""
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    x = make_x(48, 200000, torch.float32, 515)   # split kernel, 2-CTA clusters
+    y, _, _ = run_in(x)
+    assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    ref, _, _ = oracle_in(orc, x)
+    assert_close(to_f64(y), ref, torch.float32, "after timeout")
+    y2, _, _ = run_in(x)
+    assert torch.equal(y, y2)
