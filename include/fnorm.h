@@ -128,8 +128,10 @@ FNORM_API fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* 
                                          float clamp_lo, float clamp_hi, fnorm_stream_t stream);
 
 /*
- * Bytes of device workspace fnorm_batchnorm_train needs for this shape
- * (a multiple of 256; 0 when N*C*S == 0).
+ * Bytes of device workspace fnorm_batchnorm_train and
+ * fnorm_batchnorm_local_stats need for this shape: the per-(run, chunk)
+ * partial statistics plus 256 bytes for a grid-barrier counter (a multiple
+ * of 256; 0 when N*C*S == 0).
  */
 FNORM_API size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S);
 

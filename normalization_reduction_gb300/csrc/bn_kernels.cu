@@ -316,6 +316,177 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
     mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
+// ---------------------------------------------------------------------------
+// Resident form (one cooperative launch): a persistent grid of THREADS-thread
+// CTAs walks the units in memory order (unit b + i*G for CTA b), computing the
+// statistics as bn_stats_split_kernel does; the staged part (up to THREADS*NS
+// vectors) of each CTA's last unit stays in shared memory across a grid-wide
+// barrier; then every CTA normalises its units in reverse order -- the
+// resident one first, the others re-read (the most recent ones from L2).
+// The grid barrier is an arrival counter in the workspace (zeroed by the
+// host before the launch) that thread 0 of each CTA polls for at most the
+// wait limit; an expired wait sets the error word and the kernel finishes
+// (results then invalid). Partials written by other SMs are read through L2.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld_cg_f4(const float4* q) { return __ldcg(q); }
+
+template <int THREADS, int NR, int NS>
+__global__ void __launch_bounds__(THREADS, 4) bn_resident_kernel(const BnParams p) {
+  extern __shared__ __align__(16) uint4 stage[];   // THREADS * NS vectors
+  __shared__ Stat warp_part[THREADS / 32];
+  __shared__ float4 coef;
+  __shared__ uint64_t bar;
+  __shared__ uint64_t dbg_bar;
+  constexpr int RV = THREADS * NR;
+  const int tid = threadIdx.x;
+  const int64_t G = gridDim.x;
+  const int64_t units = p.N * p.C * p.chunks;
+  const int64_t mine = blockIdx.x < units ? (units - blockIdx.x + G - 1) / G : 0;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_init(&dbg_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  unsigned tph = 0;       // parity of the TMA barrier's next completion
+  bool failed = false;    // a bounded wait expired (error word set)
+
+  // ---- phase 1: statistics of every unit of this CTA
+  for (int64_t i = 0; i < mine; ++i) {
+    const BnUnit u = bn_unit(p, blockIdx.x + i * G);
+    const uint4* xv = reinterpret_cast<const uint4*>(p.x + u.run * p.S + u.lo);
+    const int nvec = static_cast<int>((u.hi - u.lo) / 4);
+    const int svec = nvec > RV ? nvec - RV : 0;
+    if (tid == 0 && svec > 0 && !failed) {
+      mbar_arrive_expect_tx(&bar, static_cast<unsigned>(svec) * 16u);
+      tma_bulk_g2s(stage, xv + RV, static_cast<unsigned>(svec) * 16u, &bar);
+    }
+    const int rvec = nvec < RV ? nvec : RV;
+    const int kr = tid < rvec ? clamp_int((rvec - tid + THREADS - 1) / THREADS, 0, NR) : 0;
+    uint4 r[NR];
+#pragma unroll
+    for (int k = 0; k < NR; ++k) r[k] = k < kr ? ld_v4(xv + k * THREADS + tid) : make_uint4(0, 0, 0, 0);
+    Stat st = tile_stat<float, NR>(r, kr * 4);
+    if (svec > 0) {
+      // an expired wait is retried once (bounded) so that the copy is not in
+      // flight when the CTA leaves; no further copies are issued
+      if (!failed && !mbar_wait_bounded(&bar, tph, p.err)) {
+        mbar_wait_bounded(&bar, tph, p.err);
+        failed = true;
+      }
+      tph ^= 1u;
+      const int ks = tid < svec ? clamp_int((svec - tid + THREADS - 1) / THREADS, 0, NS) : 0;
+#pragma unroll
+      for (int k = 0; k < NS; ++k) r[k] = k < ks ? stage[k * THREADS + tid] : make_uint4(0, 0, 0, 0);
+      st = chan_merge(st, tile_stat<float, NS>(r, ks * 4));
+    }
+    // (cta_merge's barrier also orders this unit's reads of the stage before
+    // the next unit's copy into it)
+    const Stat cta = cta_merge<THREADS>(st, warp_part);
+    if (tid == 0) *bn_partial(p, u) = make_float4(cta.n, cta.mean, cta.m2, 0.f);
+    failed = __syncthreads_or(failed);
+  }
+
+  // ---- grid-wide barrier: every partial is written before any is merged
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(p.grid_counter, 1u);
+    const unsigned target = static_cast<unsigned>(G);
+    if (atomicAdd(p.grid_counter, 0u) < target) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (atomicAdd(p.grid_counter, 0u) < target) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(p.err, kErrTimeout);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+
+  // ---- phase 2: normalise the units in reverse order, the resident one first
+  for (int64_t i = mine - 1; i >= 0; --i) {
+    const BnUnit u = bn_unit(p, blockIdx.x + i * G);
+    const int64_t off = u.run * p.S + u.lo;
+    const uint4* xv = reinterpret_cast<const uint4*>(p.x + off);
+    const int nvec = static_cast<int>((u.hi - u.lo) / 4);
+    const int svec = nvec > RV ? nvec - RV : 0;
+    const bool resident = i == mine - 1;
+    if (!resident && tid == 0 && svec > 0 && !failed) {
+      mbar_arrive_expect_tx(&bar, static_cast<unsigned>(svec) * 16u);
+      tma_bulk_g2s(stage, xv + RV, static_cast<unsigned>(svec) * 16u, &bar);
+    }
+    // the channel's statistics: its partials merged in a fixed order
+    const float4* part = p.partials + u.c * (p.N * p.chunks);
+    Stat acc = stat_empty();
+    for (int64_t j = tid; j < p.N * p.chunks; j += THREADS) {
+      const float4 v = ld_cg_f4(part + j);
+      acc = chan_merge(acc, Stat{v.x, v.y, v.z});
+    }
+    const Stat s = cta_merge<THREADS>(acc, warp_part);
+    if (tid == 0) {
+      const float var = s.m2 / s.n;
+      const float rstd = rsqrtf(var + p.eps);
+      const float g = p.gamma ? p.gamma[u.c] : 1.f;
+      const float bt = p.beta ? p.beta[u.c] : 0.f;
+      coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
+      if (u.n == 0 && u.k == 0) {
+        if (p.save_mean) p.save_mean[u.c] = s.mean;
+        if (p.save_rstd) p.save_rstd[u.c] = rstd;
+        if (p.running_mean && p.running_var) {
+          const double cnt = static_cast<double>(s.n);
+          const double mom = p.momentum;
+          const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
+          p.running_mean[u.c] = static_cast<float>((1.0 - mom) * p.running_mean[u.c] +
+                                                   mom * static_cast<double>(s.mean));
+          p.running_var[u.c] =
+              static_cast<float>((1.0 - mom) * p.running_var[u.c] + mom * unbiased);
+        }
+      }
+    }
+    __syncthreads();
+    const float4 cf = coef;
+    const int rvec = nvec < RV ? nvec : RV;
+    const int kr = tid < rvec ? clamp_int((rvec - tid + THREADS - 1) / THREADS, 0, NR) : 0;
+    uint4 r[NR];
+#pragma unroll
+    for (int k = 0; k < NR; ++k) r[k] = k < kr ? ld_v4(xv + k * THREADS + tid) : make_uint4(0, 0, 0, 0);
+    float4* yv = reinterpret_cast<float4*>(p.y + off);
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+      if (k < kr) {
+        float o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = fmaf(Elem<float>::get(r[k], q) - cf.x, cf.y, cf.z);
+        __stcs(yv + k * THREADS + tid, make_float4(o[0], o[1], o[2], o[3]));
+      }
+    }
+    if (svec > 0) {
+      if (!resident) {
+        if (!failed && !mbar_wait_bounded(&bar, tph, p.err)) {
+          mbar_wait_bounded(&bar, tph, p.err);
+          failed = true;
+        }
+        tph ^= 1u;
+      }
+      for (int j = tid; j < svec; j += THREADS) {
+        const uint4 v = stage[j];
+        float o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = fmaf(Elem<float>::get(v, q) - cf.x, cf.y, cf.z);
+        __stcs(yv + RV + j, make_float4(o[0], o[1], o[2], o[3]));
+      }
+    }
+    failed = __syncthreads_or(failed);   // the stage is read before the next copy
+  }
+  // Test hook: one CTA waits on a barrier nothing completes; the wait must
+  // expire, record the timeout in the error word and return.
+  if (p.debug_timeout && blockIdx.x == 0 && tid == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
+}
+
 // Local statistics of a rank's shard: one CTA per channel merges the
 // channel's partials in a fixed order into local_out[c] = (n, mean, M2, 0).
 template <int THREADS>
@@ -518,6 +689,30 @@ cudaError_t bn_launch(const BnParams& p, cudaStream_t stream) {
   cudaError_t e = bn_launch_stats(p, stream);
   if (e != cudaSuccess) return e;
   return bn_launch_apply_pass(p, stream);
+}
+
+cudaError_t bn_launch_resident(const BnParams& p, cudaStream_t stream) {
+  auto kernel = &bn_resident_kernel<kBnThreads, kBnSplitRegs, kBnSplitStaged>;
+  const size_t smem = static_cast<size_t>(kBnThreads) * kBnSplitStaged * 16;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBnThreads, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t units = p.N * p.C * p.chunks;
+  const int64_t cap = static_cast<int64_t>(per_sm) * device_info().sm_count;
+  if (cap <= 0) return cudaErrorCooperativeLaunchTooLarge;
+  e = cudaMemsetAsync(p.grid_counter, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units < cap ? units : cap), 1, 1);
+  cfg.blockDim = dim3(kBnThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {

@@ -417,7 +417,8 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
 // ------------------------------------------------------------ BatchNorm
 struct BnLayout {
   int64_t chunk, chunks, P;
-  size_t part_bytes;
+  size_t part_bytes;   // [C][P] float4 partials
+  size_t ws_bytes;     // partials + 256 bytes holding the resident kernel's barrier counter
 };
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -428,6 +429,7 @@ BnLayout bn_layout(int64_t N, int64_t C, int64_t S) {
   l.chunks = S > 0 ? (S + l.chunk - 1) / l.chunk : 0;
   l.P = N * l.chunks;
   l.part_bytes = round256(static_cast<size_t>(C) * l.P * 16);
+  l.ws_bytes = l.part_bytes + 256;
   return l;
 }
 
@@ -583,7 +585,7 @@ size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S) {
   int64_t t1 = 0, t2 = 0;
   if (!mul_ok(N, C, &t1) || !mul_ok(t1, S, &t2)) return 0;
   const BnLayout l = bn_layout(N, C, S);
-  return l.part_bytes;
+  return l.ws_bytes;
 }
 
 namespace {
@@ -660,9 +662,9 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
   if (!aligned(workspace, 256)) return FNORM_ERR_ALIGNMENT;
   const BnLayout l = bn_layout(N, C, S);
   if (l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
-  if (workspace_bytes < l.part_bytes) return FNORM_ERR_INVALID_ARG;
+  if (workspace_bytes < l.ws_bytes) return FNORM_ERR_INVALID_ARG;
   const size_t xb = static_cast<size_t>(total) * 4, cb = static_cast<size_t>(C) * 4,
-               wb = l.part_bytes;
+               wb = l.ws_bytes;
   const void* outs[] = {running_mean, running_var, save_mean, save_rstd};
   for (const void* o : outs)
     if (overlaps(o, cb, workspace, wb)) return FNORM_ERR_INVALID_ARG;
@@ -678,7 +680,14 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
   p.stats_cstride = l.P;
   p.stats_istride = 1;
   p.stats_count = l.P;
-  return cuda_status(bn_launch(p, reinterpret_cast<cudaStream_t>(stream)));
+  p.grid_counter = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + l.part_bytes);
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (p.vec && p.split && env("FNORM_BN_RESIDENT")) {
+    const cudaError_t e = bn_launch_resident(p, cs);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);
+    cudaGetLastError();   // grid not co-resident here: the two-launch form
+  }
+  return cuda_status(bn_launch(p, cs));
 }
 
 fnorm_status fnorm_batchnorm_eval(const float* x, float* y, const float* gamma, const float* beta,
@@ -721,10 +730,10 @@ fnorm_status fnorm_batchnorm_local_stats(const float* x, float* stats_out, int64
   if (!aligned(workspace, 256)) return FNORM_ERR_ALIGNMENT;
   const BnLayout l = bn_layout(N, C, S);
   if (l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
-  if (workspace_bytes < l.part_bytes) return FNORM_ERR_INVALID_ARG;
+  if (workspace_bytes < l.ws_bytes) return FNORM_ERR_INVALID_ARG;
   const size_t xb = static_cast<size_t>(total) * 4, sb = static_cast<size_t>(C) * 16;
-  if (overlaps(stats_out, sb, x, xb) || overlaps(stats_out, sb, workspace, l.part_bytes) ||
-      overlaps(workspace, l.part_bytes, x, xb))
+  if (overlaps(stats_out, sb, x, xb) || overlaps(stats_out, sb, workspace, l.ws_bytes) ||
+      overlaps(workspace, l.ws_bytes, x, xb))
     return FNORM_ERR_INVALID_ARG;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;

@@ -144,6 +144,7 @@ struct BnParams {
   int64_t stats_istride;
   int64_t stats_count;
   float4* local_out;    // [C] merged local statistics (local-stats call), else null
+  unsigned* grid_counter;  // resident kernel: grid-barrier arrivals (zeroed before the launch)
   bool vec;
   bool split;           // statistics pass by the register + TMA-staged kernel (vector mode)
   int debug_timeout;    // test hook (staged kernels): wait on an mbarrier nobody completes
@@ -163,6 +164,10 @@ cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);          // stats
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream);  // stats + merge
 cudaError_t bn_launch_apply(const BnParams& p, cudaStream_t stream);         // apply only
 cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream);          // eval mode, one pass
+// Single cooperative launch (statistics, grid barrier, apply) keeping part of x
+// on chip; returns cudaErrorCooperativeLaunchTooLarge when the grid cannot be
+// co-resident (the caller then uses bn_launch).
+cudaError_t bn_launch_resident(const BnParams& p, cudaStream_t stream);
 constexpr int64_t kBnEvalFlatBelow = 1024;   // runs shorter than this take the flat eval kernel
 
 // ---------------------------------------------------------------- helpers

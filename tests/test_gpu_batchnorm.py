@@ -169,3 +169,49 @@ def test_bounded_wait_timeout(orc, monkeypatch, mode):
     assert fn.fnorm_get_last_error() == fn.Status.OK
     monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
     assert_close(y.cpu().numpy(), ref, torch.float32, f"{mode} after timeout")
+
+
+@pytest.mark.parametrize("shape", [(8, 64, 126, 126), (2, 1, 100000), (300, 3, 4), (5, 7, 36),
+                                   (4, 3, 8196), (1, 2, 5), (3, 40, 16384), (64, 3, 100)])
+def test_resident_kernel(orc, monkeypatch, shape):
+    """The single cooperative launch (statistics, grid barrier, apply with
+    each CTA's last unit kept in shared memory) against the oracle: more
+    units than CTAs, fewer units than CTAs, units of several chunks, tiny
+    units, element-wise fall-back shapes (S % 4 != 0 take the two launches)."""
+    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+    x, g, b, _, _ = inputs.batchnorm(dev(), shape=shape, seed=31 + shape[1])
+    check(orc, x, g, b, what=f"resident {shape}")
+
+
+def test_resident_dirty_workspace_and_repeat(orc, monkeypatch):
+    """The barrier counter lives in the caller's workspace, which needs no
+    clearing: garbage between calls, and back-to-back calls on one stream."""
+    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+    x, g, b, _, _ = inputs.batchnorm(dev(), shape=(16, 8, 3000))
+    nbytes = fn.fnorm_batchnorm_workspace_size(16, 8, 3000)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=dev())
+    ref, _, _, _, _ = orc.batchnorm_train(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(), 2.0,
+                                          None, None, MOM, EPS)
+    for _ in range(3):
+        y, _, _ = run_bn(x, g, b, None, None, workspace=ws)
+        assert_close(y.cpu().numpy(), ref, torch.float32, "resident, dirty workspace")
+        ws.fill_(0x5A)
+    y1, _, _ = run_bn(x, g, b, None, None, workspace=ws)
+    monkeypatch.delenv("FNORM_BN_RESIDENT")
+    y2, _, _ = run_bn(x, g, b, None, None, workspace=ws)
+    assert torch.equal(y1, y2)   # same partials, same merge order: same bits as two launches
+
+
+def test_resident_timeout_hook(orc, monkeypatch):
+    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    x, g, b, _, _ = inputs.batchnorm(dev(), shape=(6, 5, 3000))
+    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    y, _, _ = run_bn(x, g, b, None, None)
+    assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    ref, _, _, _, _ = orc.batchnorm_train(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(), 2.0,
+                                          None, None, MOM, EPS)
+    assert_close(y.cpu().numpy(), ref, torch.float32, "resident after timeout")
+

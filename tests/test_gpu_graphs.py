@@ -91,6 +91,12 @@ def test_graph_batchnorm_train_and_eval():
     _capture_and_compare(run, [y, ye, sm, sr, rm, rv])
 
 
+def test_graph_batchnorm_resident(monkeypatch):
+    """The single cooperative BatchNorm launch (with its counter reset) in a graph."""
+    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+    test_graph_batchnorm_train_and_eval()
+
+
 def test_first_calls_inside_capture():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     code = ("from tests import test_gpu_graphs as t; t.test_graph_instancenorm_paths(); "
