@@ -13,6 +13,12 @@
 //   [p34] Kimi-K2.6__l1_p34 -- InstanceNorm2d(64).
 // Each page is a sequence of reasoning blocks; "block k" counts them from 1.
 //
+// Functions: InstanceNorm (float64, fp32 and bf16 storage), InstanceNorm with
+// per-channel affine parameters, the fused epilogue of [p79], BatchNorm in
+// training mode with running statistics and in eval mode (both followed by
+// the scale of [p73]), and bf16 rounding helpers. Each is pinned by the test
+// suite's pins (no function is "parity unpinned").
+//
 // Every result is the plain definition evaluated in float64 with the inputs
 // taken exactly (fp32 and bf16 values are exact in float64) and rounded once
 // to the output type at the end. Mean and variance use the textbook two-pass
