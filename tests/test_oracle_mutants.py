@@ -52,6 +52,12 @@ MUTANTS = [
     ("bn_eval_dropped_scale",
      "scale * (g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);",
      "(g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);"),
+    ("in_affine_wrong_channel",
+     "if (S > 0) moments(v.data(), S, &mean, &var);\n      const double g = gamma ? gamma[c] : 1.0;",
+     "if (S > 0) moments(v.data(), S, &mean, &var);\n      const double g = gamma ? gamma[(c + 1) % C] : 1.0;"),
+    ("bn_eval_affine_swapped",
+     "scale * (g * normalize(x[base + s], running_mean[c], running_var[c], eps) + b);",
+     "scale * (b * normalize(x[base + s], running_mean[c], running_var[c], eps) + g);"),
     ("bf16_truncate", "const double r = std::nearbyint(q);", "const double r = std::trunc(q);"),
     ("bf16_ties_away", "const double r = std::nearbyint(q);", "const double r = std::round(q);"),
 ]
