@@ -521,8 +521,8 @@ def other_configs(dev, ws, peak):
     cases = [("epilogue", lambda: Epilogue(dev), 200, 20),
              ("batchnorm", lambda: BatchNorm(dev), 20, 5),
              ("batchnorm_eval", lambda: BatchNormEval(dev), 20, 5),
-             ("instancenorm_affine", lambda: InstanceNormAffine(dev), 5, 3)]
-    cases += [(f"sweep_S{S}", (lambda S=S: Sweep(dev, S)), 10, 3) for S in inputs.SWEEP_S]
+             ("instancenorm_affine", lambda: InstanceNormAffine(dev), 20, 5)]
+    cases += [(f"sweep_S{S}", (lambda S=S: Sweep(dev, S)), 20, 5) for S in inputs.SWEEP_S]
     for key, make, steps, warm in cases:
         wl = make()
         total_ms, step_ms, _ = time_workload(wl, steps, warm, ws)
