@@ -150,8 +150,47 @@ __global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnPara
     mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
+// The channel's statistics, merged in a fixed order from `count` partials
+// part[i * istride] (read through L2 when LOADCG: partials written by other
+// SMs of the same launch), as the apply coefficients (mean, A, B) for every
+// thread of the CTA; with `first` the CTA also writes the saved statistics
+// and updates the running statistics (count = all values of the channel, all
+// ranks; unbiased variance for the running estimate).
+template <int THREADS, bool LOADCG>
+__device__ __forceinline__ float4 bn_channel_coef(const BnParams& p, int64_t c, const float4* part,
+                                                  int64_t count, int64_t istride, bool first,
+                                                  Stat* warp_part, float4* coef) {
+  Stat acc = stat_empty();
+  for (int64_t i = threadIdx.x; i < count; i += THREADS) {
+    const float4 v = LOADCG ? __ldcg(part + i * istride) : part[i * istride];
+    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
+  }
+  const Stat s = cta_merge<THREADS>(acc, warp_part);
+  if (threadIdx.x == 0) {
+    const float var = s.m2 / s.n;
+    const float rstd = rsqrtf(var + p.eps);
+    const float g = p.gamma ? p.gamma[c] : 1.f;
+    const float bt = p.beta ? p.beta[c] : 0.f;
+    *coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
+    if (first) {
+      if (p.save_mean) p.save_mean[c] = s.mean;
+      if (p.save_rstd) p.save_rstd[c] = rstd;
+      if (p.running_mean && p.running_var) {
+        const double cnt = static_cast<double>(s.n);
+        const double mom = p.momentum;
+        const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
+        p.running_mean[c] = static_cast<float>((1.0 - mom) * p.running_mean[c] +
+                                               mom * static_cast<double>(s.mean));
+        p.running_var[c] = static_cast<float>((1.0 - mom) * p.running_var[c] + mom * unbiased);
+      }
+    }
+  }
+  __syncthreads();
+  return *coef;
+}
+
 template <int THREADS, int U, bool VEC>
-__global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
+__global__ void __launch_bounds__(THREADS, 4) bn_apply_kernel(const BnParams p) {
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ float4 coef;
   // units in the reverse of memory order: the statistics pass read the last
@@ -180,34 +219,9 @@ __global__ void __launch_bounds__(THREADS) bn_apply_kernel(const BnParams p) {
 
   // channel statistics: the channel's partials (or the ranks' statistics)
   // merged in a fixed order
-  const float4* part = p.stats + c * p.stats_cstride;
-  Stat acc = stat_empty();
-  for (int64_t i = threadIdx.x; i < p.stats_count; i += THREADS) {
-    const float4 v = part[i * p.stats_istride];
-    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
-  }
-  const Stat s = cta_merge<THREADS>(acc, warp_part);
-  if (threadIdx.x == 0) {
-    const float var = s.m2 / s.n;
-    const float rstd = rsqrtf(var + p.eps);
-    const float g = p.gamma ? p.gamma[c] : 1.f;
-    const float bt = p.beta ? p.beta[c] : 0.f;
-    coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
-    if (b == 0) {
-      if (p.save_mean) p.save_mean[c] = s.mean;
-      if (p.save_rstd) p.save_rstd[c] = rstd;
-      if (p.running_mean && p.running_var) {
-        const double cnt = static_cast<double>(s.n);   // all values of the channel (all ranks)
-        const double mom = p.momentum;
-        const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
-        p.running_mean[c] = static_cast<float>((1.0 - mom) * p.running_mean[c] +
-                                               mom * static_cast<double>(s.mean));
-        p.running_var[c] = static_cast<float>((1.0 - mom) * p.running_var[c] + mom * unbiased);
-      }
-    }
-  }
-  __syncthreads();
-  const float4 cf = coef;
+  const float4 cf = bn_channel_coef<THREADS, false>(p, c, p.stats + c * p.stats_cstride,
+                                                    p.stats_count, p.stats_istride, b == 0,
+                                                    warp_part, &coef);
 
   const int tid = threadIdx.x;
   constexpr int64_t TILE = static_cast<int64_t>(THREADS) * U * 4;
@@ -268,34 +282,9 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
     mbar_arrive_expect_tx(&bar, static_cast<unsigned>(nvec) * 16u);
     tma_bulk_g2s(stage, p.x + off, static_cast<unsigned>(nvec) * 16u, &bar);
   }
-  const float4* part = p.stats + u.c * p.stats_cstride;
-  Stat acc = stat_empty();
-  for (int64_t i = tid; i < p.stats_count; i += THREADS) {
-    const float4 v = part[i * p.stats_istride];
-    acc = chan_merge(acc, Stat{v.x, v.y, v.z});
-  }
-  const Stat s = cta_merge<THREADS>(acc, warp_part);
-  if (tid == 0) {
-    const float var = s.m2 / s.n;
-    const float rstd = rsqrtf(var + p.eps);
-    const float g = p.gamma ? p.gamma[u.c] : 1.f;
-    const float bt = p.beta ? p.beta[u.c] : 0.f;
-    coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
-    if (u.n == 0 && u.k == 0) {
-      if (p.save_mean) p.save_mean[u.c] = s.mean;
-      if (p.save_rstd) p.save_rstd[u.c] = rstd;
-      if (p.running_mean && p.running_var) {
-        const double cnt = static_cast<double>(s.n);
-        const double mom = p.momentum;
-        const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
-        p.running_mean[u.c] = static_cast<float>((1.0 - mom) * p.running_mean[u.c] +
-                                                 mom * static_cast<double>(s.mean));
-        p.running_var[u.c] = static_cast<float>((1.0 - mom) * p.running_var[u.c] + mom * unbiased);
-      }
-    }
-  }
-  __syncthreads();
-  const float4 cf = coef;
+  const float4 cf = bn_channel_coef<THREADS, false>(p, u.c, p.stats + u.c * p.stats_cstride,
+                                                    p.stats_count, p.stats_istride,
+                                                    u.n == 0 && u.k == 0, warp_part, &coef);
   if (nvec > 0) {
     // a wait that gives up has flagged the error; it is retried once (bounded)
     // so that the copy is not in flight when the CTA leaves
@@ -328,8 +317,6 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
 // wait limit; an expired wait sets the error word and the kernel finishes
 // (results then invalid). Partials written by other SMs are read through L2.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float4 ld_cg_f4(const float4* q) { return __ldcg(q); }
-
 template <int THREADS, int NR, int NS>
 __global__ void __launch_bounds__(THREADS, 4) bn_resident_kernel(const BnParams p) {
   extern __shared__ __align__(16) uint4 stage[];   // THREADS * NS vectors
@@ -420,35 +407,9 @@ __global__ void __launch_bounds__(THREADS, 4) bn_resident_kernel(const BnParams 
       tma_bulk_g2s(stage, xv + RV, static_cast<unsigned>(svec) * 16u, &bar);
     }
     // the channel's statistics: its partials merged in a fixed order
-    const float4* part = p.partials + u.c * (p.N * p.chunks);
-    Stat acc = stat_empty();
-    for (int64_t j = tid; j < p.N * p.chunks; j += THREADS) {
-      const float4 v = ld_cg_f4(part + j);
-      acc = chan_merge(acc, Stat{v.x, v.y, v.z});
-    }
-    const Stat s = cta_merge<THREADS>(acc, warp_part);
-    if (tid == 0) {
-      const float var = s.m2 / s.n;
-      const float rstd = rsqrtf(var + p.eps);
-      const float g = p.gamma ? p.gamma[u.c] : 1.f;
-      const float bt = p.beta ? p.beta[u.c] : 0.f;
-      coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
-      if (u.n == 0 && u.k == 0) {
-        if (p.save_mean) p.save_mean[u.c] = s.mean;
-        if (p.save_rstd) p.save_rstd[u.c] = rstd;
-        if (p.running_mean && p.running_var) {
-          const double cnt = static_cast<double>(s.n);
-          const double mom = p.momentum;
-          const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
-          p.running_mean[u.c] = static_cast<float>((1.0 - mom) * p.running_mean[u.c] +
-                                                   mom * static_cast<double>(s.mean));
-          p.running_var[u.c] =
-              static_cast<float>((1.0 - mom) * p.running_var[u.c] + mom * unbiased);
-        }
-      }
-    }
-    __syncthreads();
-    const float4 cf = coef;
+    const float4 cf = bn_channel_coef<THREADS, true>(p, u.c, p.partials + u.c * (p.N * p.chunks),
+                                                     p.N * p.chunks, 1, u.n == 0 && u.k == 0,
+                                                     warp_part, &coef);
     const int rvec = nvec < RV ? nvec : RV;
     const int kr = tid < rvec ? clamp_int((rvec - tid + THREADS - 1) / THREADS, 0, NR) : 0;
     uint4 r[NR];
