@@ -160,7 +160,9 @@ FNORM_API size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S)
  * Requires N*S >= 2 (the unbiased estimate needs two values).
  * x is read twice (statistics, then normalisation in reverse order so that
  * the tail of the first pass is still in L2) and y written once; two kernel
- * launches.
+ * launches. Runs of at most 16 values (S <= 16, e.g. BatchNorm over [N, C])
+ * take a column form instead: per-column statistics over blocks of rows, a
+ * per-channel merge, then the normalisation (three launches).
  */
 FNORM_API fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma, const float* beta,
                                    float scale, float* running_mean, float* running_var,

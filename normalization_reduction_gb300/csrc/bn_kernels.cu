@@ -448,6 +448,75 @@ __global__ void __launch_bounds__(THREADS, 4) bn_resident_kernel(const BnParams 
   if (p.debug_timeout && blockIdx.x == 0 && tid == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
+// ---------------------------------------------------------------------------
+// Column form for short runs (S <= kBnColMaxS, e.g. BatchNorm over [N, C]):
+// x is read as N rows of W = C*S values. Units of one run would be a handful
+// of values each, so instead
+//   1. bn_col_stats_kernel -- a CTA covers THREADS columns x kBnColRows rows;
+//      each thread takes the exact two-pass statistics of its column's rows
+//      -> partial[j][row block] (channel c owns columns [c*S, (c+1)*S), so its
+//      partials are contiguous);
+//   2. bn_col_merge_kernel -- one CTA per channel merges them in a fixed
+//      order into (mean, A, B), the saved and the running statistics;
+//   3. bn_col_apply_kernel -- elementwise, each thread walks one column down
+//      the rows with its channel's coefficients.
+// ---------------------------------------------------------------------------
+template <int THREADS, int R>
+__global__ void __launch_bounds__(THREADS) bn_col_stats_kernel(const BnParams p) {
+  const int64_t W = p.C * p.S;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x;
+  const int64_t nrb = (p.N + R - 1) / R;
+  pdl_wait();
+  for (int64_t rb = blockIdx.y; rb < nrb; rb += gridDim.y) {
+    if (j < W) {
+      const int64_t r0 = rb * R;
+      const int rows = static_cast<int>(p.N - r0 < R ? p.N - r0 : R);
+      float v[R];
+#pragma unroll
+      for (int k = 0; k < R; ++k) v[k] = k < rows ? __ldg(p.x + (r0 + k) * W + j) : 0.f;
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < R; ++k) sum += k < rows ? v[k] - v[0] : 0.f;
+      const float n = static_cast<float>(rows);
+      const float mean = v[0] + sum / n;
+      float m2 = 0.f;
+#pragma unroll
+      for (int k = 0; k < R; ++k) {
+        const float d = v[k] - mean;
+        m2 += k < rows ? d * d : 0.f;
+      }
+      p.partials[j * nrb + rb] = make_float4(n, mean, m2, 0.f);
+    }
+  }
+  pdl_trigger();
+}
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) bn_col_merge_kernel(const BnParams p) {
+  __shared__ Stat warp_part[THREADS / 32];
+  __shared__ float4 coef;
+  const int64_t c = blockIdx.x;
+  const int64_t count = p.S * ((p.N + kBnColRows - 1) / kBnColRows);
+  pdl_wait();
+  const float4 cf = bn_channel_coef<THREADS, false>(p, c, p.partials + c * count, count, 1, true,
+                                                    warp_part, &coef);
+  if (threadIdx.x == 0) p.local_out[c] = cf;   // the channel's (mean, A, B)
+  pdl_trigger();
+}
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) bn_col_apply_kernel(const BnParams p) {
+  const int64_t W = p.C * p.S;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x;
+  pdl_wait();
+  if (j < W) {
+    const float4 cf = p.local_out[j / p.S];
+    for (int64_t r = blockIdx.y; r < p.N; r += gridDim.y)
+      p.y[r * W + j] = fmaf(__ldg(p.x + r * W + j) - cf.x, cf.y, cf.z);
+  }
+  pdl_trigger();
+}
+
 // Local statistics of a rank's shard: one CTA per channel merges the
 // channel's partials in a fixed order into local_out[c] = (n, mean, M2, 0).
 template <int THREADS>
@@ -674,6 +743,24 @@ cudaError_t bn_launch_resident(const BnParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+cudaError_t bn_launch_columns(const BnParams& p, cudaStream_t stream) {
+  const int64_t W = p.C * p.S;
+  const int64_t nrb = (p.N + kBnColRows - 1) / kBnColRows;
+  const unsigned gx = static_cast<unsigned>((W + kBnThreads - 1) / kBnThreads);
+  const unsigned gy_stats = static_cast<unsigned>(nrb < 65535 ? nrb : 65535);
+  cudaError_t e = bn_launch_one(&bn_col_stats_kernel<kBnThreads, kBnColRows>,
+                                dim3(gx, gy_stats, 1), stream, p);
+  if (e != cudaSuccess) return e;
+  e = bn_launch_one(&bn_col_merge_kernel<kBnThreads>, dim3(static_cast<unsigned>(p.C), 1, 1),
+                    stream, p);
+  if (e != cudaSuccess) return e;
+  // enough row groups per column tile to fill the GPU
+  const int64_t want = (static_cast<int64_t>(device_info().sm_count) * 8 + gx - 1) / gx;
+  const int64_t gy = want < p.N ? (want < 65535 ? want : 65535) : p.N;
+  return bn_launch_one(&bn_col_apply_kernel<kBnThreads>,
+                       dim3(gx, static_cast<unsigned>(gy > 0 ? gy : 1), 1), stream, p);
 }
 
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {

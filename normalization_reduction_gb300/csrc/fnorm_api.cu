@@ -418,7 +418,8 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
 struct BnLayout {
   int64_t chunk, chunks, P;
   size_t part_bytes;   // [C][P] float4 partials
-  size_t ws_bytes;     // partials + 256 bytes holding the resident kernel's barrier counter
+  size_t col_part_bytes = 0;   // short runs: [C*S][row blocks] partials (coefficients follow)
+  size_t ws_bytes;     // the larger layout + 256 bytes holding the resident kernel's barrier counter
 };
 
 size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -430,6 +431,13 @@ BnLayout bn_layout(int64_t N, int64_t C, int64_t S) {
   l.P = N * l.chunks;
   l.part_bytes = round256(static_cast<size_t>(C) * l.P * 16);
   l.ws_bytes = l.part_bytes + 256;
+  if (S > 0 && S <= kBnColMaxS) {
+    // column form: [C*S][row blocks] partials, then [C] coefficients
+    const int64_t nrb = (N + kBnColRows - 1) / kBnColRows;
+    l.col_part_bytes = round256(static_cast<size_t>(C) * S * nrb * 16);
+    const size_t col_bytes = l.col_part_bytes + round256(static_cast<size_t>(C) * 16);
+    if (col_bytes + 256 > l.ws_bytes) l.ws_bytes = col_bytes + 256;
+  }
   return l;
 }
 
@@ -680,8 +688,12 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
   p.stats_cstride = l.P;
   p.stats_istride = 1;
   p.stats_count = l.P;
-  p.grid_counter = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + l.part_bytes);
+  p.grid_counter = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + l.ws_bytes - 256);
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (l.col_part_bytes > 0 && !env("FNORM_BN_NO_COLUMNS")) {
+    p.local_out = reinterpret_cast<float4*>(static_cast<char*>(workspace) + l.col_part_bytes);
+    return cuda_status(bn_launch_columns(p, cs));
+  }
   if (p.vec && p.split && env("FNORM_BN_RESIDENT")) {
     const cudaError_t e = bn_launch_resident(p, cs);
     if (e != cudaErrorCooperativeLaunchTooLarge) return cuda_status(e);

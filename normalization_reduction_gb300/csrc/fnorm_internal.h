@@ -164,6 +164,11 @@ cudaError_t bn_launch(const BnParams& p, cudaStream_t stream);          // stats
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream);  // stats + merge
 cudaError_t bn_launch_apply(const BnParams& p, cudaStream_t stream);         // apply only
 cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream);          // eval mode, one pass
+// Short runs (S <= kBnColMaxS): column statistics, channel merge, apply. Uses
+// p.partials ([C*S][row blocks]) and p.local_out ([C] coefficients).
+cudaError_t bn_launch_columns(const BnParams& p, cudaStream_t stream);
+constexpr int64_t kBnColMaxS = 16;   // runs this short take the column form (training)
+constexpr int kBnColRows = 32;       // rows per column-statistics partial
 // Single cooperative launch (statistics, grid barrier, apply) keeping part of x
 // on chip; returns cudaErrorCooperativeLaunchTooLarge when the grid cannot be
 // co-resident (the caller then uses bn_launch).

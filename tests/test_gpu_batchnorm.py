@@ -215,3 +215,16 @@ def test_resident_timeout_hook(orc, monkeypatch):
                                           None, None, MOM, EPS)
     assert_close(y.cpu().numpy(), ref, torch.float32, "resident after timeout")
 
+
+@pytest.mark.parametrize("shape", [(4096, 64, 1), (1000, 3, 7), (33, 17, 3), (31, 5, 16),
+                                   (100000, 2, 1), (1, 2, 16), (2, 1, 1), (65, 300, 2)])
+@pytest.mark.parametrize("columns", ["1", "0"], ids=["columns", "units"])
+def test_short_runs(orc, monkeypatch, shape, columns):
+    """Runs of at most 16 values (BatchNorm over [N, C] and small maps): the
+    column form (column statistics over row blocks, channel merge, apply) and
+    the per-unit form agree with the oracle, running statistics included."""
+    if columns == "0":
+        monkeypatch.setenv("FNORM_BN_NO_COLUMNS", "1")
+    x, g, b, _, _ = inputs.batchnorm(dev(), shape=shape, seed=41 + shape[0])
+    check(orc, x, g, b, what=f"short runs {shape} columns={columns}")
+
