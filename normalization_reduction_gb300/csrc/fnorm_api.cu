@@ -168,6 +168,8 @@ bool in_forced_plan(InPlan* plan) {
     plan->path = InPath::kStream;
     plan->threads = kStreamThreads;
     plan->nv = kStreamUnroll;
+    if (const char* u = env("FNORM_STREAM_UNROLL"))
+      plan->nv = std::atoi(u) == kStreamUnrollFew ? kStreamUnrollFew : kStreamUnroll;
     plan->cluster = a;
     return true;
   }
@@ -261,8 +263,15 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
   } else {
     plan.path = InPath::kStream;
     plan.threads = kStreamThreads;
-    plan.nv = kStreamUnroll;
-    plan.cluster = 8;
+    // few slices: 16 CTAs per slice (non-portable clusters) when 8 would leave
+    // most SMs idle, and more loads in flight per thread
+    const bool few = NC * 8 < device_info().sm_count;
+    // 8 loads of 16 bytes per thread for fp32 input or few slices; 4 for bf16
+    // input with many slices (measured: the same ~32 values per thread)
+    plan.nv = (few || tin == 0) ? kStreamUnrollFew : kStreamUnroll;
+    plan.cluster = few ? 16 : 8;
+    if (const char* u = env("FNORM_STREAM_UNROLL"))
+      plan.nv = std::atoi(u) == kStreamUnrollFew ? kStreamUnrollFew : kStreamUnroll;
   }
 
   int cap = in_capacity(tin, tout, plan);

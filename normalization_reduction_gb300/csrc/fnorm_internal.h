@@ -55,7 +55,8 @@ constexpr int kSplitShapes[][3] = {{128, 8, 8}, {256, 8, 8}, {512, 8, 8}, {1024,
                                    {1024, 8, 0}};
 constexpr int kGroupShapes[][2] = {{8, 1}, {8, 4}, {32, 2}, {32, 4}, {32, 8}};
 constexpr int kStreamThreads = 512;
-constexpr int kStreamUnroll = 4;
+constexpr int kStreamUnroll = 4;       // 16-byte loads per thread per tile (many slices)
+constexpr int kStreamUnrollFew = 8;    // ... when few slices keep few CTAs busy
 constexpr int kMaxCluster = 16;
 
 // Defined in in_kernels.cuh and instantiated per (Tin, Tout) in in_*.cu.

@@ -744,9 +744,12 @@ static void* pick_kernel(const InPlan& plan) {
 #undef FNORM_GRP
       return nullptr;
     case InPath::kStream:
-      if (plan.threads == kStreamThreads)
+      if (plan.threads == kStreamThreads && plan.nv == kStreamUnroll)
         return reinterpret_cast<void*>(
             &in_stream_kernel<Tin, Tout, kStreamThreads, kStreamUnroll, VEC>);
+      if (plan.threads == kStreamThreads && plan.nv == kStreamUnrollFew)
+        return reinterpret_cast<void*>(
+            &in_stream_kernel<Tin, Tout, kStreamThreads, kStreamUnrollFew, VEC>);
       return nullptr;
     case InPath::kSplit:
       if (!VEC) return nullptr;

@@ -221,3 +221,17 @@ def test_bounded_wait_timeout(orc, monkeypatch):
     assert_close(to_f64(y), ref, torch.float32, "after timeout")
     y2, _, _ = run_in(x)
     assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("shape,dt", [((1, 3, 2048, 2048), torch.float32),
+                                      ((2, 1, 1500, 1500), torch.bfloat16),
+                                      ((1, 1, 1 << 21, 1), torch.bfloat16)])
+def test_few_long_slices(orc, shape, dt):
+    """A few slices longer than a cluster holds (the stream form; 16-CTA
+    clusters when 8 would leave most SMs idle), in the default plan."""
+    N, C = shape[0], shape[1]
+    S = shape[2] * shape[3]
+    x = make_x(N * C, S, dt, 77 + S)
+    y, _, _ = run_in(x, dt)
+    ref, _, _ = oracle_in(orc, x)
+    assert_close(to_f64(y), ref, dt, f"few long slices {shape}")
