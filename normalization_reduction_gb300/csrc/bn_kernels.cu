@@ -631,6 +631,21 @@ __global__ void __launch_bounds__(THREADS, 3) bn_eval_staged_kernel(const BnPara
     mbar_wait_bounded(&dbg_bar, 0, p.err);
 }
 
+// Very short runs (S <= kBnColMaxS, e.g. [N, C]): x as N rows of C*S values;
+// each thread walks one column down the rows with its channel's coefficients.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) bn_eval_col_kernel(const BnParams p) {
+  const int64_t W = p.C * p.S;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x;
+  pdl_wait();
+  if (j < W) {
+    const float4 cf = bn_eval_coef(p, j / p.S);
+    for (int64_t r = blockIdx.y; r < p.N; r += gridDim.y)
+      p.y[r * W + j] = fmaf(__ldg(p.x + r * W + j) - cf.x, cf.y, cf.z);
+  }
+  pdl_trigger();
+}
+
 // Short runs (S < kBnEvalFlatBelow): a grid-stride loop over vectors (or
 // elements), each finding its channel from its index.
 template <int THREADS, bool VEC>
@@ -781,6 +796,14 @@ cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream) {
     }
     return p.vec ? bn_launch_one(&bn_eval_kernel<kBnThreads, kBnUnroll, true>, grid, stream, p)
                  : bn_launch_one(&bn_eval_kernel<kBnThreads, kBnUnroll, false>, grid, stream, p);
+  }
+  if (p.S <= kBnColMaxS) {
+    const int64_t W = p.C * p.S;
+    const unsigned gx = static_cast<unsigned>((W + kBnThreads - 1) / kBnThreads);
+    const int64_t want = (static_cast<int64_t>(device_info().sm_count) * 8 + gx - 1) / gx;
+    const int64_t gy = want < p.N ? (want < 65535 ? want : 65535) : p.N;
+    return bn_launch_one(&bn_eval_col_kernel<kBnThreads>,
+                         dim3(gx, static_cast<unsigned>(gy > 0 ? gy : 1), 1), stream, p);
   }
   const int64_t units = p.N * p.C * (p.vec ? p.S / 4 : p.S);
   const int64_t cap = static_cast<int64_t>(device_info().sm_count) * (2048 / kBnThreads);
