@@ -517,6 +517,45 @@ __global__ void __launch_bounds__(THREADS) bn_col_apply_kernel(const BnParams p)
   pdl_trigger();
 }
 
+// Multi-rank apply for short runs (column form): each thread folds the R
+// ranks' statistics of its column's channel in rank order (the same fold on
+// every rank, so every rank obtains the same bits), then walks its column;
+// the thread of the channel's first column in the first row group writes the
+// saved statistics and updates the running statistics.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) bn_col_apply_stats_kernel(const BnParams p) {
+  const int64_t W = p.C * p.S;
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * THREADS + threadIdx.x;
+  pdl_wait();
+  if (j < W) {
+    const int64_t c = j / p.S;
+    Stat s = stat_empty();
+    for (int64_t r = 0; r < p.stats_count; ++r) {
+      const float4 v = p.stats[c * p.stats_cstride + r * p.stats_istride];
+      s = chan_merge(s, Stat{v.x, v.y, v.z});
+    }
+    const float rstd = rsqrtf(s.m2 / s.n + p.eps);
+    const float g = p.gamma ? p.gamma[c] : 1.f;
+    const float bt = p.beta ? p.beta[c] : 0.f;
+    const float4 cf = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
+    if (blockIdx.y == 0 && j == c * p.S) {
+      if (p.save_mean) p.save_mean[c] = s.mean;
+      if (p.save_rstd) p.save_rstd[c] = rstd;
+      if (p.running_mean && p.running_var) {
+        const double cnt = static_cast<double>(s.n);
+        const double mom = p.momentum;
+        const double unbiased = static_cast<double>(s.m2) / (cnt - 1.0);
+        p.running_mean[c] = static_cast<float>((1.0 - mom) * p.running_mean[c] +
+                                               mom * static_cast<double>(s.mean));
+        p.running_var[c] = static_cast<float>((1.0 - mom) * p.running_var[c] + mom * unbiased);
+      }
+    }
+    for (int64_t r = blockIdx.y; r < p.N; r += gridDim.y)
+      p.y[r * W + j] = fmaf(__ldg(p.x + r * W + j) - cf.x, cf.y, cf.z);
+  }
+  pdl_trigger();
+}
+
 // Local statistics of a rank's shard: one CTA per channel merges the
 // channel's partials in a fixed order into local_out[c] = (n, mean, M2, 0).
 template <int THREADS>
@@ -776,6 +815,37 @@ cudaError_t bn_launch_columns(const BnParams& p, cudaStream_t stream) {
   const int64_t gy = want < p.N ? (want < 65535 ? want : 65535) : p.N;
   return bn_launch_one(&bn_col_apply_kernel<kBnThreads>,
                        dim3(gx, static_cast<unsigned>(gy > 0 ? gy : 1), 1), stream, p);
+}
+
+// Column grid for short runs: THREADS columns per CTA, enough row groups to
+// fill the GPU.
+static dim3 bn_col_grid(const BnParams& p) {
+  const int64_t W = p.C * p.S;
+  const unsigned gx = static_cast<unsigned>((W + kBnThreads - 1) / kBnThreads);
+  const int64_t want = (static_cast<int64_t>(device_info().sm_count) * 8 + gx - 1) / gx;
+  const int64_t gy = want < p.N ? (want < 65535 ? want : 65535) : p.N;
+  return dim3(gx > 0 ? gx : 1, static_cast<unsigned>(gy > 0 ? gy : 1), 1);
+}
+
+cudaError_t bn_launch_columns_local_stats(const BnParams& p, cudaStream_t stream) {
+  const int64_t W = p.C * p.S;
+  const int64_t nrb = (p.N + kBnColRows - 1) / kBnColRows;
+  const unsigned gx = static_cast<unsigned>((W + kBnThreads - 1) / kBnThreads);
+  cudaError_t e = bn_launch_one(&bn_col_stats_kernel<kBnThreads, kBnColRows>,
+                                dim3(gx, static_cast<unsigned>(nrb < 65535 ? nrb : 65535), 1),
+                                stream, p);
+  if (e != cudaSuccess) return e;
+  BnParams q = p;   // the channel's partials are contiguous: [c][S * row blocks]
+  q.stats = p.partials;
+  q.stats_cstride = p.S * nrb;
+  q.stats_istride = 1;
+  q.stats_count = p.S * nrb;
+  return bn_launch_one(&bn_merge_kernel<kBnThreads>, dim3(static_cast<unsigned>(p.C), 1, 1),
+                       stream, q);
+}
+
+cudaError_t bn_launch_columns_apply_stats(const BnParams& p, cudaStream_t stream) {
+  return bn_launch_one(&bn_col_apply_stats_kernel<kBnThreads>, bn_col_grid(p), stream, p);
 }
 
 cudaError_t bn_launch_local_stats(const BnParams& p, cudaStream_t stream) {

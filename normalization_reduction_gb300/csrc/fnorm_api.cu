@@ -767,6 +767,8 @@ fnorm_status fnorm_batchnorm_local_stats(const float* x, float* stats_out, int64
   p.stats_istride = 1;
   p.stats_count = l.P;
   p.local_out = reinterpret_cast<float4*>(stats_out);
+  if (l.col_part_bytes > 0 && !env("FNORM_BN_NO_COLUMNS"))
+    return cuda_status(bn_launch_columns_local_stats(p, reinterpret_cast<cudaStream_t>(stream)));
   return cuda_status(bn_launch_local_stats(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -802,6 +804,8 @@ fnorm_status fnorm_batchnorm_apply_stats(const float* x, float* y, const float* 
   p.stats_cstride = 1;
   p.stats_istride = C;
   p.stats_count = R;
+  if (!stats_only && S <= kBnColMaxS && !env("FNORM_BN_NO_COLUMNS"))
+    return cuda_status(bn_launch_columns_apply_stats(p, reinterpret_cast<cudaStream_t>(stream)));
   return cuda_status(bn_launch_apply(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 

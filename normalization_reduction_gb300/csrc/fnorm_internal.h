@@ -168,6 +168,8 @@ cudaError_t bn_launch_eval(const BnParams& p, cudaStream_t stream);          // 
 // Short runs (S <= kBnColMaxS): column statistics, channel merge, apply. Uses
 // p.partials ([C*S][row blocks]) and p.local_out ([C] coefficients).
 cudaError_t bn_launch_columns(const BnParams& p, cudaStream_t stream);
+cudaError_t bn_launch_columns_local_stats(const BnParams& p, cudaStream_t stream);
+cudaError_t bn_launch_columns_apply_stats(const BnParams& p, cudaStream_t stream);
 constexpr int64_t kBnColMaxS = 16;   // runs this short take the column form (training)
 constexpr int kBnColRows = 32;       // rows per column-statistics partial
 // Single cooperative launch (statistics, grid barrier, apply) keeping part of x

@@ -28,10 +28,16 @@ def local_stats(shard):
 
 
 @pytest.mark.parametrize("splits", [[2, 2], [3, 5], [4, 0, 3], [1, 1, 1, 1, 4]])
-def test_emulated_ranks_match_whole_batch(orc, splits):
-    shape = (sum(splits), 6, 9, 11)
+@pytest.mark.parametrize("spatial", [(9, 11), (1,), (3,), (4, 4)],
+                         ids=["S99", "S1", "S3", "S16"])
+def test_emulated_ranks_match_whole_batch(orc, splits, spatial):
+    """Runs of more than 16 values take the per-unit kernels, shorter runs the
+    column kernels (column statistics; rank-ordered fold per column)."""
+    shape = (sum(splits) * (64 if len(spatial) == 1 else 1), 6) + spatial
+    splits = [n * (64 if len(spatial) == 1 else 1) for n in splits]
     x, g, b, rm, rv = inputs.batchnorm(dev(), shape=shape, seed=55 + len(splits))
-    C, S = shape[1], shape[2] * shape[3]
+    C = shape[1]
+    S = int(np.prod(spatial))
     shards, lo = [], 0
     for n in splits:
         shards.append(x[lo:lo + n].contiguous())
@@ -51,7 +57,7 @@ def test_emulated_ranks_match_whole_batch(orc, splits):
                                                    g.cpu().numpy(), b.cpu().numpy(), SCALE,
                                                    rm.cpu().numpy(), rv.cpu().numpy(), MOM, EPS)
     got = torch.cat(outs).cpu().numpy().reshape(ref.shape)
-    assert_close(got, ref, torch.float32, f"splits {splits}")
+    assert_close(got, ref, torch.float32, f"splits {splits} spatial {spatial}")
     for rm_r, rv_r in zip(rms, rvs):
         assert np.max(np.abs(rm_r.cpu().numpy() - rmo)) <= 1e-6
         assert np.max(np.abs(rv_r.cpu().numpy() - rvo)) <= 2e-6
