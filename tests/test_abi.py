@@ -3,6 +3,7 @@ point, and rejects bad arguments before touching the GPU."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -187,3 +188,42 @@ def test_batchnorm_eval_validation(lib, kw, expect):
              N=2, C=3, S=64, stream=0)
     a.update(kw)
     assert _rc(lambda: fn.fnorm_batchnorm_eval(**a)) == expect
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "fnorm.h"
+int call_all(void* x, void* y, float* g, float* m, long long* a, void* ws, fnorm_stream_t s) {
+  fnorm_status st = fnorm_instancenorm(x, y, 2, 3, 64, FNORM_F32, FNORM_BF16, 1e-5f, 0, 0, s);
+  st = fnorm_instancenorm_affine(x, y, g, g, 2, 3, 64, FNORM_BF16, FNORM_F32, 1e-5f, 0, 0, s);
+  st = fnorm_instancenorm_epilogue((const float*)x, m, (float*)y, (int64_t*)a, 2, 3, 64, 1e-5f,
+                                   -1.f, 1.f, s);
+  size_t wb = fnorm_batchnorm_workspace_size(2, 3, 64);
+  st = fnorm_batchnorm_train((const float*)x, (float*)y, g, g, 2.f, g, g, 0.1f, 1e-5f, 0, 0,
+                             2, 3, 64, ws, wb, s);
+  st = fnorm_batchnorm_eval((const float*)x, (float*)y, g, g, 2.f, g, g, 1e-5f, 2, 3, 64, s);
+  st = fnorm_batchnorm_local_stats((const float*)x, g, 2, 3, 64, ws, wb, s);
+  st = fnorm_batchnorm_apply_stats((const float*)x, (float*)y, g, 1, g, g, 2.f, g, g, 0.1f,
+                                   1e-5f, 0, 0, 2, 3, 64, s);
+  st = fnorm_batchnorm_train_noalloc((const float*)x, (float*)y, g, g, 2.f, g, g, 0.1f, 1e-5f,
+                                     0, 0, 2, 3, 64, s);
+  printf("%s %d %d\n", fnorm_status_string(st), (int)fnorm_get_last_error(), fnorm_version());
+  return (int)st;
+}
+"""
+
+
+def test_header_is_plain_c(tmp_path, lib):
+    """A C caller of every entry point compiles against include/fnorm.h with
+    gcc (no CUDA headers) and links against libfnorm.so."""
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    inc = os.path.dirname(HEADER)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", inc, "-c", str(src), "-o",
+                        str(tmp_path / "caller.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    so = tmp_path / "libcaller.so"
+    r = subprocess.run(["gcc", "-shared", str(tmp_path / "caller.o"), "-o", str(so),
+                        fn.LIBRARY, "-Wl,--no-undefined", "-Wl,--allow-shlib-undefined"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
