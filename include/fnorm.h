@@ -214,6 +214,8 @@ FNORM_API fnorm_status fnorm_batchnorm_eval(const float* x, float* y, const floa
  * count (unbiased estimate; the merged count must be >= 2). Arguments as for
  * fnorm_batchnorm_train; no workspace. A rank whose shard is empty (N*S == 0)
  * still merges stats_all and updates its running and saved statistics.
+ * Runs of at most 16 values (S <= 16) take column forms in both steps (every
+ * rank of a group uses the same form, since S is the same on every rank).
  */
 FNORM_API fnorm_status fnorm_batchnorm_local_stats(const float* x, float* stats_out, int64_t N,
                                                    int64_t C, int64_t S, void* workspace,
