@@ -122,6 +122,10 @@ __global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnPara
   }
   __syncthreads();
   pdl_wait();
+  // The apply launch may be scheduled as soon as every CTA of this grid has
+  // started (its CTAs then wait in griddepcontrol.wait for this grid to
+  // complete), which hides its launch behind the last wave of this one.
+  pdl_trigger();
   if (tid == 0 && svec > 0) {
     mbar_arrive_expect_tx(&bar, static_cast<unsigned>(svec) * 16u);
     tma_bulk_g2s(stage, xv + RV, static_cast<unsigned>(svec) * 16u, &bar);
@@ -143,7 +147,6 @@ __global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnPara
   }
   const Stat cta = cta_merge<THREADS>(st, warp_part);
   if (tid == 0) *bn_partial(p, u) = make_float4(cta.n, cta.mean, cta.m2, 0.f);
-  pdl_trigger();
   // Test hook: one CTA waits on a barrier nothing completes; the wait must
   // expire, record the timeout in the error word and return.
   if (p.debug_timeout && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
