@@ -314,6 +314,10 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
   if (csize > 1) cluster_sync();
   else __syncthreads();
   pdl_wait();
+  // The next launch may be scheduled once every CTA of this grid has started
+  // (the grid never exceeds the co-resident capacity); its CTAs take free
+  // slots and wait in griddepcontrol.wait, which hides its launch.
+  pdl_trigger();
 
   bool xfailed = false;
   int it = 0;
