@@ -211,8 +211,9 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
     // Split-resident. Up to 4096 slots (64 KiB of input) a CTA of 64..512
     // threads holds the slice in registers (8 slots per thread); up to 8192
     // slots a 512-thread CTA holds 8 slots per thread in registers and 8 in
-    // TMA-staged shared memory (two CTAs per SM); longer slices take clusters
-    // of such CTAs. FNORM_SPLIT_SHAPE=threads:nr:ns overrides the CTA shape.
+    // TMA-staged shared memory (two CTAs per SM); up to 65536 slots clusters
+    // of up to 16 such 256-thread CTAs (four per SM), beyond that clusters of
+    // 512-thread CTAs. FNORM_SPLIT_SHAPE=threads:nr:ns overrides the CTA shape.
     plan.path = InPath::kSplit;
     plan.nv = 8;
     plan.ns = 0;
@@ -221,7 +222,16 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
     else if (slots <= 1024) plan.threads = 128;
     else if (slots <= 2048) plan.threads = 256;
     else if (slots <= 4096) plan.threads = 512;
-    else {
+    else if (slots <= 8192) {
+      plan.threads = 512;
+      plan.ns = 8;
+    } else if (slots <= 16 * 4096) {
+      // 256-thread CTAs of 64 KiB in clusters of up to 16 (four CTAs per SM):
+      // 2-4 % faster than 512-thread CTAs of 128 KiB in half the clusters
+      plan.threads = 256;
+      plan.ns = 8;
+      plan.cluster = static_cast<int>((slots + 4095) / 4096);
+    } else {
       plan.threads = 512;
       plan.ns = 8;
       plan.cluster = static_cast<int>((slots + 8191) / 8192);
@@ -275,10 +285,11 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
   }
 
   int cap = in_capacity(tin, tout, plan);
-  if (cap <= 0 && plan.path == InPath::kSplit && plan.cluster > 8 && !env("FNORM_FORCE_PATH")) {
+  if (cap <= 0 && plan.path == InPath::kSplit && plan.cluster > 8 && !env("FNORM_FORCE_PATH") &&
+      !env("FNORM_SPLIT_SHAPE")) {
     // 16-CTA clusters not available: twice the chunk per CTA, half the CTAs
-    plan.threads = 1024;
-    plan.cluster = static_cast<int>((slots + 16383) / 16384);
+    plan.threads *= 2;
+    plan.cluster = static_cast<int>((slots + plan.threads * 16 - 1) / (plan.threads * 16));
     cap = in_capacity(tin, tout, plan);
   }
   if (cap <= 0 && plan.path != InPath::kGroup && plan.cluster > 8 && !env("FNORM_FORCE_PATH")) {
