@@ -42,9 +42,9 @@ L2_BYTES = 126 * 1024 * 1024
 # DRAM bytes (read + write) per launch of each workload's dominant kernel from
 # one ncu capture (profiles/*.md); None until measured for the current kernel.
 NCU_TRAFFIC = {
-    # profiles/in_split_kernel__instancenorm_fp32_112x64x512x512.md: 1.073793 GB read +
-    # 1.022873 GB written for 1024 slices, scaled by 7 to the 7168-slice launch
-    "instancenorm2d_fp32_112x64x512x512": 14676662000,
+    # profiles/in_split_kernel__instancenorm_fp32_112x64x512x512.md: 1.073823 GB read +
+    # 1.018198 GB written for 1024 slices, scaled by 7 to the 7168-slice launch
+    "instancenorm2d_fp32_112x64x512x512": 14644147000,
     # profiles/bn_eval_staged_kernel__batchnorm_eval_fp32_128x64x126x126.md (full size)
     "batchnorm2d_eval_fp32_128x64x126x126": 984366848,
     # profiles/bn_kernels__batchnorm_train_fp32_128x64x126x126.md: both launches of a step
