@@ -2,7 +2,7 @@
 x once, write y once) and the fraction of the measured HBM peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-extra]
+                    [--workload NAME] [--shape N,C,H,W] [--no-extra]
 
 One step is one call of the hot path over one batch of the workload. The
 default workload is InstanceNorm2d forward, fp32, x[112,64,512,512] ~ N(0,1)
