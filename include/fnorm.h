@@ -119,9 +119,11 @@ FNORM_API fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const f
  *           lowest index among equal maxima (NULL to skip).
  *   clamp   clamp_lo <= clamp_hi; clamp(t) = min(max(t, lo), hi).
  * y and argmax must not overlap x, m or each other.
- * When a sample's C slices fit on chip in one cluster (C*S*4 bytes up to
- * about 3 MiB, C <= 1024, x/y/argmax 16-byte aligned and S a multiple of 4)
- * x is read once; otherwise each slice is read twice.
+ * With x/y/argmax 16-byte aligned and S a multiple of 4, a cluster of CTAs
+ * handles each sample in one launch: x is read from HBM once for the
+ * statistics, and the output pass re-reads it from L2 (the leading part of
+ * each channel's range from shared memory), so HBM sees about one read of x
+ * while the input fits in L2. Other shapes stream each slice twice.
  */
 FNORM_API fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
                                          int64_t N, int64_t C, int64_t S, float eps,
@@ -130,8 +132,9 @@ FNORM_API fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* 
 /*
  * Bytes of device workspace fnorm_batchnorm_train and
  * fnorm_batchnorm_local_stats need for this shape: the per-(run, chunk)
- * partial statistics plus 256 bytes for a grid-barrier counter (a multiple
- * of 256; 0 when N*C*S == 0).
+ * partial statistics (for runs of at most 16 values, per-column partials and
+ * per-channel coefficients, whichever layout is larger) plus 256 bytes for a
+ * grid-barrier counter (a multiple of 256; 0 when N*C*S == 0).
  */
 FNORM_API size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S);
 
