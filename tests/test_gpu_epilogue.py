@@ -86,6 +86,14 @@ def test_l2_keep_sizes(orc, monkeypatch, shape, keep, cl):
     check(orc, x, m, what=f"keep {keep} {shape} cl {cl}")
 
 
+@pytest.mark.parametrize("shape", [(300, 16, 1000), (200, 8, 12600), (513, 3, 256)])
+def test_more_samples_than_clusters(orc, shape):
+    """More samples than co-resident clusters: each persistent cluster takes
+    several samples in turn (alternating exchange slots and barrier phases)."""
+    x, m = inputs.epilogue(dev(), shape=shape, seed=600 + shape[0])
+    check(orc, x, m, what=f"many samples {shape}")
+
+
 @pytest.mark.parametrize("cl", [1, 2, 4, 8])
 def test_ring_cluster_sizes(orc, monkeypatch, cl):
     monkeypatch.setenv("FNORM_EPI_RING", "1")
