@@ -159,6 +159,21 @@ def test_in_place(orc):
     assert_close(to_f64(x), ref, torch.float32, "in place")
 
 
+@pytest.mark.parametrize("S,dt,NC", [(262144, torch.float32, 80), (65536, torch.bfloat16, 400),
+                                     (200, torch.bfloat16, 3000), (600000, torch.float32, 5),
+                                     (12600, torch.float32, 700)])
+def test_in_place_every_family(orc, S, dt, NC):
+    """y == x for the split kernel (registers + staged part prefetched for the
+    next slice, 16-CTA clusters, more slices than clusters), the group kernel
+    and the stream form: every slice is read before it is written."""
+    x = make_x(NC, S, dt, 45 + S)
+    ref, _, _ = oracle_in(orc, x)
+    c = code(dt)
+    fn.fnorm_instancenorm(x, x, 1, NC, S, c, c, EPS, None, None)
+    torch.cuda.synchronize()
+    assert_close(to_f64(x), ref, dt, f"in place S={S}")
+
+
 def test_constant_slices_exact_zero():
     """Constant slices of awkward values (not exactly summable) give exact zeros."""
     for S in (3, 1000, 12600, 262144):
