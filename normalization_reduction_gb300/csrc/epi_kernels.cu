@@ -5,27 +5,30 @@
 // channel dimension; output [N, D, H, W]).
 //
 // The page plans two kernels (per-(n,c) statistics, then one thread per output
-// position looping over channels), which reads the convolution output twice.
-// Here one thread-block cluster owns one sample n, and CTA r of the cluster
-// owns a contiguous range of output positions FOR ALL C CHANNELS:
-//  * the CTA stages x[n, c, range] for every c in shared memory with C TMA
-//    bulk copies (cp.async.bulk + mbarrier, bounded waits);
-//  * each warp forms the partial statistics of some channels over the range
-//    (exact two-pass over 16-value register tiles, Chan merges);
-//  * the C partials are pushed with st.async into every CTA of the cluster,
-//    completing on the receiver's mbarrier; every CTA merges the partials of
-//    each channel in rank order (bit-identical results in all CTAs);
-//  * each thread then produces its positions from local shared memory:
-//    the max over c of z_c and, optionally, its channel index.
-// HBM sees one read of x and one write of y, and only C*cluster*16 bytes per
-// CTA cross distributed shared memory. The statistics are formed on x, and the
-// multiplier is folded in exactly by the affine identity
+// position looping over channels), which reads the convolution output twice
+// from HBM. Here one launch does both: a thread-block cluster owns a sample n,
+// and CTA r of the cluster owns a contiguous range of output positions FOR
+// ALL C CHANNELS. The statistics are formed on x and the multiplier is folded
+// in exactly by the affine identity
 //   IN(m x) = (x - mean_x) * m / sqrt(m^2 var_x + eps),
 // so z_c = m_c * clamp((x - mean_x) * a_c, lo, hi) with a_c = m_c*rsqrt(m_c^2 var_x + eps).
-//
-// A second kernel covers inputs that do not fit (or are not 16-byte aligned):
-// one cluster per sample, CTAs owning whole channels, reading each slice twice
-// from global memory with element-wise loads.
+// Kernels (the plan picks the first that applies):
+//  * epi_range_l2_kernel (default; 16-byte aligned, S % 4 == 0): each warp
+//    reduces some channels over the CTA's range from HBM (exact two-pass over
+//    register tiles, Chan merges), keeping the first KS vectors of each
+//    channel's range in shared memory; the C partials are pushed with st.async
+//    into every CTA of the cluster (completing on the receiver's mbarrier, all
+//    CTAs merge in rank order: bit-identical results); the output pass takes
+//    the kept vectors from shared memory and re-reads the rest of the range,
+//    which the statistics pass has just brought into L2 (the whole input of
+//    the page's shape, 103 MB, fits in L2), and writes max_c z_c (+ argmax).
+//  * epi_range_kernel (FNORM_EPI_STAGED=1): the range is staged in shared
+//    memory by TMA bulk copies, double-buffered across samples.
+//  * epi_ring_kernel (FNORM_EPI_RING=1): a producer warp streams the range
+//    through a TMA ring twice (statistics, then outputs).
+//  * epi_stream_kernel (inputs that are not 16-byte aligned or too wide):
+//    one cluster per sample, CTAs owning whole channels, each slice read twice
+//    with element-wise loads.
 #include "fnorm_device.cuh"
 #include "fnorm_internal.h"
 #include "in_kernels.cuh"
