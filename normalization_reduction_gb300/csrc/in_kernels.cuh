@@ -1,31 +1,38 @@
-// in_kernels.cuh -- InstanceNorm forward kernels (affine = False).
+// in_kernels.cuh -- InstanceNorm forward kernels (with optional per-channel
+// affine parameters).
 //
 // What is computed (page Kimi-K2.6__l1_p34, blocks 1-2; the same statistics
 // as the InstanceNorm3d step of page Kimi-K2.6__l2_p79, block 1): for every
 // (n,c) slice of S contiguous elements, the mean and the biased variance, then
-// y = (x - mean) * rsqrt(var + eps).
+// y = (x - mean) * rsqrt(var + eps), or with affine parameters
+// y = (x - mean) * (rsqrt(var + eps) * gamma_c) + beta_c.
 //
 // How (GB300 design, not the pages' H100 plan of one 512-thread block per slice
 // reading the slice twice):
-//  * The slice is held in REGISTERS while its statistics are formed, so it is
-//    read from HBM once and written once. Each thread owns NV 16-byte slots
-//    (4 fp32 or 8 bf16 values) loaded with 128-bit coalesced loads.
-//  * Per thread, an exact two-pass mean/M2 over its own registers (shifted by
-//    its first value so a constant slice gives M2 = 0 and the exact mean), then
+//  * The slice is held ON CHIP while its statistics are formed, so it is read
+//    from HBM once and written once. Each thread owns 16-byte slots (4 fp32 or
+//    8 bf16 values) in registers, loaded with 128-bit coalesced loads, and in
+//    the split form also slots in shared memory filled by a TMA bulk copy
+//    that is issued for the next slice while the current one is processed.
+//  * Per thread, an exact two-pass mean/M2 over its own values (shifted by its
+//    first value so a constant slice gives M2 = 0 and the exact mean), then
 //    the Chan pairwise merge: warp shuffles -> shared memory across warps ->
-//    distributed shared memory across the CTAs of a thread-block cluster when
-//    one slice spans several CTAs (up to 16, i.e. 2 MiB of input per slice).
+//    the CTAs of a thread-block cluster when one slice spans several CTAs (up
+//    to 16, i.e. 2 MiB of input per slice; partials pushed with st.async).
 //    Every merge runs in a fixed tree, so results are reproducible, and every
 //    CTA of a cluster computes bit-identical statistics.
-//  * Three shapes of the same idea:
+//  * Kernel shapes:
 //      group    -- G lanes of a warp per slice (S up to 256 slots);
-//      resident -- one CTA or one cluster per slice;
-//      stream   -- fallback for slices beyond cluster capacity: one cluster per
-//                  slice, statistics pass then a normalisation pass that walks
-//                  the slice backwards so its most recently read part is still
-//                  in L2.
-//  * Grids are persistent: as many CTAs/clusters as fit on the 152 SMs at
-//    once, each looping over slices.
+//      split    -- one CTA or one cluster per slice, registers (+ staged
+//                  shared memory): the default for 16-byte-aligned slices;
+//      resident -- one CTA or one cluster per slice, registers only, with
+//                  element-wise access (unaligned inputs, S % vector != 0);
+//      stream   -- slices beyond cluster capacity: one cluster per slice,
+//                  statistics pass then a normalisation pass that walks the
+//                  slice backwards so its most recently read part is still in
+//                  L2.
+//  * Grids are persistent: as many CTAs/clusters as fit on the SMs at once,
+//    each looping over slices.
 #pragma once
 
 #include "fnorm_device.cuh"
