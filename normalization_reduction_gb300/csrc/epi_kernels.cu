@@ -282,9 +282,103 @@ __device__ __forceinline__ void epi_take(const uint4& u, const float4& k, int c,
   }
 }
 
+// Shifted sums of one lane's fp32 values: with K the lane's first value,
+// d = x - K, S = sum d, Q = sum d^2, the lane's statistics are mean = K + S/n,
+// M2 = Q - S^2/n. K is one of the values, so (K - mean)^2 <= M2 and
+// Q <= (n + 1) M2: the cancellation grows with n, which the plan bounds
+// (kEpiOnePassMaxPer vectors per CTA range, at most 160 values per lane; longer
+// ranges take exact two-pass tiles). Three floating-point operations per value
+// instead of the four of an exact two-pass tile plus a merge per tile, issued
+// as pairs (__fadd2_rn / __ffma2_rn, two fp32 lanes per instruction);
+// x - K is x + (-K), which is exact.
+struct LaneSums {
+  float2 s01, s23, q01, q23;
+  float2 nk;   // (-K, -K)
+  int cnt;     // vectors accumulated
+};
+
+__device__ __forceinline__ LaneSums lane_sums_begin(float K) {
+  LaneSums a;
+  a.s01 = a.s23 = a.q01 = a.q23 = make_float2(0.f, 0.f);
+  a.nk = make_float2(-K, -K);
+  a.cnt = 0;
+  return a;
+}
+
+// Adds r's values (cnt is counted by the caller).
+__device__ __forceinline__ void lane_sums_acc(LaneSums& a, const uint4& r) {
+  const float2 d01 = __fadd2_rn(make_float2(__uint_as_float(r.x), __uint_as_float(r.y)), a.nk);
+  const float2 d23 = __fadd2_rn(make_float2(__uint_as_float(r.z), __uint_as_float(r.w)), a.nk);
+  a.s01 = __fadd2_rn(a.s01, d01);
+  a.s23 = __fadd2_rn(a.s23, d23);
+  a.q01 = __ffma2_rn(d01, d01, a.q01);
+  a.q23 = __ffma2_rn(d23, d23, a.q23);
+}
+
+__device__ __forceinline__ Stat lane_sums_stat(const LaneSums& a) {
+  if (a.cnt == 0) return stat_empty();
+  const float n = 4.f * static_cast<float>(a.cnt);
+  const float S = (a.s01.x + a.s01.y) + (a.s23.x + a.s23.y);
+  const float Q = (a.q01.x + a.q01.y) + (a.q23.x + a.q23.y);
+  return Stat{n, S / n - a.nk.x, fmaxf(Q - S * (S / n), 0.f)};
+}
+
+// max(a, b, c) in one instruction (three-input max); like fmaxf it ignores a
+// NaN operand, so it equals fmaxf(fmaxf(a, b), c).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Saturating form of the clamp, for the output without the index: with
+// w = h - l, min(max(v A + B, l), h) = l + w sat(v A/w + (B - l)/w), where sat
+// clamps to [0, 1] in the fused multiply-add (and maps NaN to 0, as the
+// min/max form maps it to l); w = 0 gives l. Two instructions per value
+// instead of three; the value may differ from the min/max form in the last
+// bits (the rounding of A/w and (B - l)/w, and of the second FMA).
+__device__ __forceinline__ float4 epi_sat_coef(const float4& k) {
+  const float w = k.w - k.z;
+  if (!(w > 0.f)) return make_float4(0.f, 0.f, k.z, 0.f);
+  return make_float4(k.x / w, (k.y - k.z) / w, k.z, w);
+}
+
+__device__ __forceinline__ float epi_zsat(float v, const float4& k) {
+  float t;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(t) : "f"(v), "f"(k.x), "f"(k.y));
+  return fmaf(t, k.w, k.z);
+}
+
+// best = max(best, z_a, z_b) for two channels (saturating coefficients).
+__device__ __forceinline__ void epi_take_pair_sat(const uint4& ua, const float4& ka, const uint4& ub,
+                                                  const float4& kb, float (&best)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    best[j] = fmax3(best[j], epi_zsat(Elem<float>::get(ua, j), ka), epi_zsat(Elem<float>::get(ub, j), kb));
+}
+
+// z of one channel: the min/max clamp with the index, the saturating one without.
+template <bool WANT_ARG>
+__device__ __forceinline__ float epi_z(float v, const float4& k) {
+  return WANT_ARG ? epi_zc(v, k) : epi_zsat(v, k);
+}
+
+template <bool WANT_ARG>
+__device__ __forceinline__ void epi_take_any(const uint4& u, const float4& k, int c, float (&best)[4],
+                                             int (&arg)[4]) {
+  if (WANT_ARG) {
+    epi_take<true>(u, k, c, best, arg);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) best[j] = fmaxf(best[j], epi_zsat(Elem<float>::get(u, j), k));
+  }
+}
+
 // KEEP >= 0 fixes the kept vectors per channel at compile time (the common
-// full-size case); KEEP < 0 takes p.keep.
-template <int THREADS, bool WANT_ARG, int KEEP>
+// full-size case); KEEP < 0 takes p.keep. ONEPASS selects the shifted lane
+// sums for the statistics (ranges of at most kEpiOnePassMaxPer vectors), else
+// exact two-pass tiles.
+template <int THREADS, bool WANT_ARG, int KEEP, bool ONEPASS>
 __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParams p) {
   extern __shared__ __align__(16) float4 dyn[];
   __shared__ __align__(8) uint64_t xbar[2];
@@ -332,6 +426,8 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
     for (int c = warp; c < C; c += NWARP) {
       const uint4* xc = xn + int64_t(c) * nv4 + lane;
       Stat acc = stat_empty();
+      LaneSums ls = lane_sums_begin(
+          ONEPASS && lane < vr ? __ldg(reinterpret_cast<const float*>(xc)) : 0.f);
       int t = 0;
       for (; t + 32 * U <= vr; t += 32 * U) {   // full tiles
         uint4 r[U];
@@ -342,9 +438,15 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
           for (int u = 0; u < U; ++u)
             if (u * 32 + lane < KS) keep[c * KS + u * 32 + lane] = r[u];
         }
-        acc = chan_merge(acc, tile_stat_full<float, U>(r));
+        if (ONEPASS) {
+#pragma unroll
+          for (int u = 0; u < U; ++u) lane_sums_acc(ls, r[u]);
+          ls.cnt += U;
+        } else {
+          acc = chan_merge(acc, tile_stat_full<float, U>(r));
+        }
       }
-      if (t < vr) {                              // ragged tail
+      if (vr - t > 4 * 32) {                     // long ragged tail: one predicated tile
         uint4 r[U];
         int nvalid = 0;
 #pragma unroll
@@ -354,8 +456,33 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
           nvalid += v ? 4 : 0;
           if (t == 0 && v && u * 32 + lane < KS) keep[c * KS + u * 32 + lane] = r[u];
         }
-        acc = chan_merge(acc, tile_stat<float, U>(r, nvalid));
+        if (ONEPASS) {
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (t + u * 32 + lane < vr) {
+              lane_sums_acc(ls, r[u]);
+              ++ls.cnt;
+            }
+        } else {
+          acc = chan_merge(acc, tile_stat<float, U>(r, nvalid));
+        }
+        t = vr;
       }
+      for (; t < vr; t += 32) {                  // short tail: one vector per lane
+        const bool v = t + lane < vr;
+        uint4 r1[1];
+        r1[0] = v ? ld_v4(xc + t) : make_uint4(0, 0, 0, 0);
+        if (v && t + lane < KS) keep[c * KS + t + lane] = r1[0];
+        if (ONEPASS) {
+          if (v) {
+            lane_sums_acc(ls, r1[0]);
+            ++ls.cnt;
+          }
+        } else {
+          acc = chan_merge(acc, tile_stat<float, 1>(r1, v ? 4 : 0));
+        }
+      }
+      if (ONEPASS) acc = lane_sums_stat(ls);
       acc = warp_merge<32>(acc);
       const float4 v = make_float4(__shfl_sync(kFullMask, acc.n, 0), __shfl_sync(kFullMask, acc.mean, 0),
                                    __shfl_sync(kFullMask, acc.m2, 0), 0.f);
@@ -375,7 +502,10 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
         s = Stat{v.x, v.y, v.z};
       }
       s = warp_merge<16>(s);
-      if (lane == 0) coef[c] = epi_out_coef(s, __ldg(p.m + c), p.eps, p.lo, p.hi);
+      if (lane == 0) {
+        const float4 k = epi_out_coef(s, __ldg(p.m + c), p.eps, p.lo, p.hi);
+        coef[c] = WANT_ARG ? k : epi_sat_coef(k);
+      }
     }
     __syncthreads();
     const int vk = vr < KS ? vr : KS;
@@ -386,9 +516,13 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
         const uint4 u = keep[v];
         const float4 k = coef[0];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) best[j] = epi_zc(Elem<float>::get(u, j), k);
+        for (int j = 0; j < 4; ++j) best[j] = epi_z<WANT_ARG>(Elem<float>::get(u, j), k);
       }
-      for (int c = 1; c < C; ++c) epi_take<WANT_ARG>(keep[c * KS + v], coef[c], c, best, arg);
+      int c = 1;
+      if (!WANT_ARG)
+        for (; c + 2 <= C; c += 2)
+          epi_take_pair_sat(keep[c * KS + v], coef[c], keep[(c + 1) * KS + v], coef[c + 1], best);
+      for (; c < C; ++c) epi_take_any<WANT_ARG>(keep[c * KS + v], coef[c], c, best, arg);
       const int64_t pos = (v0 + v) * 4;
       __stcs(reinterpret_cast<float4*>(p.y + n * S + pos), make_float4(best[0], best[1], best[2], best[3]));
       if (WANT_ARG) {
@@ -405,17 +539,22 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
         const uint4 u = __ldcs(xv);
         const float4 k = coef[0];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) best[j] = epi_zc(Elem<float>::get(u, j), k);
+        for (int j = 0; j < 4; ++j) best[j] = epi_z<WANT_ARG>(Elem<float>::get(u, j), k);
       }
       int c = 1;
       for (; c + G <= C; c += G) {
         uint4 u[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) u[g] = __ldcs(xv + int64_t(c + g) * nv4);
+        if (WANT_ARG) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) epi_take<WANT_ARG>(u[g], coef[c + g], c + g, best, arg);
+          for (int g = 0; g < G; ++g) epi_take<WANT_ARG>(u[g], coef[c + g], c + g, best, arg);
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; g += 2) epi_take_pair_sat(u[g], coef[c + g], u[g + 1], coef[c + g + 1], best);
+        }
       }
-      for (; c < C; ++c) epi_take<WANT_ARG>(__ldcs(xv + int64_t(c) * nv4), coef[c], c, best, arg);
+      for (; c < C; ++c) epi_take_any<WANT_ARG>(__ldcs(xv + int64_t(c) * nv4), coef[c], c, best, arg);
       const int64_t pos = (v0 + v) * 4;
       __stcs(reinterpret_cast<float4*>(p.y + n * S + pos), make_float4(best[0], best[1], best[2], best[3]));
       if (WANT_ARG) {
@@ -739,11 +878,18 @@ static EpiKernelFn epi_kernel(const EpiPlan& plan) {
       return plan.want_arg ? &epi_range_kernel<kEpiThreads, true>
                            : &epi_range_kernel<kEpiThreads, false>;
     case EpiPath::kRangeL2:
-      if (plan.keep == kEpiKeepMax)
-        return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, kEpiKeepMax>
-                             : &epi_range_l2_kernel<kEpiThreads, false, kEpiKeepMax>;
-      return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, -1>
-                           : &epi_range_l2_kernel<kEpiThreads, false, -1>;
+      if (plan.keep == kEpiKeepMax) {
+        if (plan.onepass)
+          return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, kEpiKeepMax, true>
+                               : &epi_range_l2_kernel<kEpiThreads, false, kEpiKeepMax, true>;
+        return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, kEpiKeepMax, false>
+                             : &epi_range_l2_kernel<kEpiThreads, false, kEpiKeepMax, false>;
+      }
+      if (plan.onepass)
+        return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, -1, true>
+                             : &epi_range_l2_kernel<kEpiThreads, false, -1, true>;
+      return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, -1, false>
+                           : &epi_range_l2_kernel<kEpiThreads, false, -1, false>;
     case EpiPath::kRing:
       return plan.want_arg ? &epi_ring_kernel<true> : &epi_ring_kernel<false>;
     case EpiPath::kStream: return &epi_stream_kernel<kEpiThreads>;

@@ -330,8 +330,9 @@ int epi_query(const void* arg) { return epi_max_active_clusters(static_cast<cons
 
 int epi_capacity(const EpiPlan& plan) {
   char key[128];
-  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%d|%d|%zu", static_cast<int>(plan.path),
-                plan.threads, plan.cluster, plan.want_arg ? 1 : 0, plan.ring_t, plan.smem);
+  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%d|%d|%zu|%d|%d", static_cast<int>(plan.path),
+                plan.threads, plan.cluster, plan.want_arg ? 1 : 0, plan.ring_t, plan.smem,
+                plan.keep == kEpiKeepMax ? 1 : 0, plan.onepass ? 1 : 0);
   EpiQuery q{plan};
   return occupancy_cached(key, epi_query, &q);
 }
@@ -407,7 +408,8 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
     if (const char* k = env("FNORM_EPI_KEEP")) keep = std::atoi(k) < keep ? std::atoi(k) : keep;
     if (keep < 0) keep = 0;
     EpiPlan cand{EpiPath::kRangeL2, kEpiThreads, cl_eff, per, argmax != nullptr, 0,
-                 epi_range_l2_smem(C, cl_eff, keep), 0, keep};
+                 epi_range_l2_smem(C, cl_eff, keep), 0, keep,
+                 per <= kEpiOnePassMaxPer && !env("FNORM_EPI_TWOPASS")};
     if (cl >= 1 && cl <= kMaxCluster && epi_capacity(cand) > 0) {
       plan = cand;
       have = true;
@@ -427,9 +429,9 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   if (env("FNORM_DEBUG_PLAN"))
     std::fprintf(stderr,
                  "fnorm_instancenorm_epilogue plan: path=%d cluster=%d per=%lld ring_t=%d keep=%d "
-                 "smem=%zu grid=%d capacity=%d\n",
+                 "onepass=%d smem=%zu grid=%d capacity=%d\n",
                  static_cast<int>(plan.path), plan.cluster, static_cast<long long>(plan.per),
-                 plan.ring_t, plan.keep, plan.smem, plan.grid, cap);
+                 plan.ring_t, plan.keep, plan.onepass ? 1 : 0, plan.smem, plan.grid, cap);
   *out = plan;
   return FNORM_OK;
 }

@@ -101,6 +101,7 @@ struct EpiPlan {
   size_t smem;   // dynamic shared memory bytes
   int grid;      // CTAs (multiple of cluster)
   int keep;      // L2 path: position vectors per channel kept on chip
+  bool onepass;  // L2 path: shifted lane sums for the statistics (per <= kEpiOnePassMaxPer)
 };
 
 constexpr int kEpiThreads = 256;
@@ -114,6 +115,9 @@ size_t epi_range_l2_smem(int64_t C, int cluster, int keep);
 // L2 path: the leading position vectors of each channel of a CTA's range that
 // stay in shared memory from the statistics pass to the output pass.
 constexpr int kEpiKeepMax = 160;
+// L2 path: CTA ranges of at most this many position vectors (at most 40 per
+// lane, 160 values) take the shifted one-pass lane sums for the statistics.
+constexpr int64_t kEpiOnePassMaxPer = 1280;
 constexpr int kEpiKeepBudget = 40960;   // bytes (keeps the CTA under 48 KB of dynamic smem)
 size_t epi_ring_smem(int64_t C, int ring_t, int cluster);
 size_t epi_stream_smem(int64_t C, int cluster);

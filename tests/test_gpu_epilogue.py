@@ -197,3 +197,66 @@ def test_bounded_wait_timeout(orc, monkeypatch):
     ref, _, _ = orc.epilogue(x.cpu().numpy().reshape(2, 16, -1), m.cpu().numpy(), EPS)
     assert_close(y.cpu().numpy(), ref, torch.float32, "after timeout")
     check(orc, x, m, what="after timeout")
+
+
+def check_no_arg(orc, x, m, lo=-1.0, hi=1.0, what=""):
+    """The output without the index (the saturating form of the clamp)
+    against the oracle."""
+    y, _ = run_epi(x, m, lo, hi, want_arg=False)
+    N, C = x.shape[0], x.shape[1]
+    ref, _, _ = orc.epilogue(x.cpu().numpy().reshape(N, C, -1), m.cpu().numpy(), EPS, lo, hi)
+    assert_close(y.cpu().numpy(), ref, torch.float32, what)
+    return y
+
+
+@pytest.mark.parametrize("lo,hi", [(-1.0, 1.0), (-0.5, 0.25), (0.0, 0.0), (-3.0, 3.0), (0.5, 2.0)])
+def test_clamp_bounds_no_index(orc, lo, hi):
+    """Both signs of the multiplier (the clamp interval m*[lo, hi] flips for
+    m < 0), a zero multiplier and an empty interval, without the index."""
+    x, _ = inputs.epilogue(dev(), shape=(3, 16, 1000))
+    m = torch.linspace(-1.5, 1.5, 16, device=dev())
+    m[7] = 0.0
+    check_no_arg(orc, x, m, lo, hi, what=f"clamp {lo},{hi} no index")
+
+
+def test_saturated_channels_no_index(orc):
+    """Clamped outliers without the index: the largest |m_c| wins with 2.0
+    (up to the rounding of the saturating clamp)."""
+    N, C, S = 2, 4, 4096
+    x = torch.zeros(N, C, S, device=dev())
+    x[:, :, 17] = 1000.0
+    x[:, :, 18:] = torch.randn(N, C, S - 18, device=dev()) * 0.01
+    m = torch.tensor([0.5, 1.5, -2.0, 1.25], device=dev())
+    y = check_no_arg(orc, x, m, what="saturation, no index")
+    assert torch.allclose(y[:, 17], torch.full_like(y[:, 17], 2.0), rtol=0, atol=1e-6)
+
+
+@pytest.mark.parametrize("S", [4096, 20480, 40000])
+@pytest.mark.parametrize("want_arg", [True, False], ids=["index", "no_index"])
+@pytest.mark.parametrize("form", ["default", "twopass"])
+def test_outliers_at_lane_shifts(orc, monkeypatch, S, want_arg, form):
+    """For CTA ranges of at most 1280 vectors (S = 20480 with the default
+    4-CTA split: 40 vectors per lane) the statistics are per-lane sums shifted
+    by the lane's first value; longer ranges, and every range with
+    FNORM_EPI_TWOPASS=1, take exact two-pass tiles. An outlier at the shift is
+    the worst case for the shifted sums: put one at the first value of every
+    lane of every CTA range, on data with a large offset; the outputs must
+    still match the oracle."""
+    if form == "twopass":
+        monkeypatch.setenv("FNORM_EPI_TWOPASS", "1")
+    N, C = 2, 3
+    g = torch.Generator().manual_seed(4242 + S)
+    x = (torch.randn(N, C, S, generator=g) * 0.5 + 50.0)
+    nv4 = S // 4
+    per = (nv4 + 3) // 4
+    for r in range(4):
+        for lane in range(32):
+            v = r * per + lane
+            if v < min(nv4, (r + 1) * per):
+                x[:, :, 4 * v] = 50.0 + 400.0 * (1 if lane % 2 else -1)
+    x = x.to(dev())
+    m = torch.tensor([0.75, -1.25, 2.0], device=dev())
+    if want_arg:
+        check(orc, x, m, what=f"lane-shift outliers S={S} {form}")
+    else:
+        check_no_arg(orc, x, m, what=f"lane-shift outliers S={S} {form} no index")
