@@ -14,14 +14,18 @@
 // so z_c = m_c * clamp((x - mean_x) * a_c, lo, hi) with a_c = m_c*rsqrt(m_c^2 var_x + eps).
 // Kernels (the plan picks the first that applies):
 //  * epi_range_l2_kernel (default; 16-byte aligned, S % 4 == 0): each warp
-//    reduces some channels over the CTA's range from HBM (exact two-pass over
-//    register tiles, Chan merges), keeping the first KS vectors of each
-//    channel's range in shared memory; the C partials are pushed with st.async
-//    into every CTA of the cluster (completing on the receiver's mbarrier, all
-//    CTAs merge in rank order: bit-identical results); the output pass takes
-//    the kept vectors from shared memory and re-reads the rest of the range,
-//    which the statistics pass has just brought into L2 (the whole input of
-//    the page's shape, 103 MB, fits in L2), and writes max_c z_c (+ argmax).
+//    reduces some channels over the CTA's range from HBM (per-lane sums
+//    shifted by the lane's first value for ranges of at most
+//    kEpiOnePassMaxPer vectors, exact two-pass register tiles beyond; Chan
+//    merges), keeping the first KS vectors of each channel's range in shared
+//    memory; the C partials are pushed with st.async into every CTA of the
+//    cluster (completing on the receiver's mbarrier, all CTAs merge in rank
+//    order: bit-identical results); the output pass takes the kept vectors
+//    from shared memory and re-reads the rest of the range, which the
+//    statistics pass has just brought into L2 (the whole input of the page's
+//    shape, 103 MB, fits in L2), and writes max_c z_c (+ argmax; without the
+//    index the clamp is a saturating FMA and channels go in pairs through a
+//    three-input max).
 //  * epi_range_kernel (FNORM_EPI_STAGED=1): the range is staged in shared
 //    memory by TMA bulk copies, double-buffered across samples.
 //  * epi_ring_kernel (FNORM_EPI_RING=1): a producer warp streams the range
