@@ -127,9 +127,9 @@ int in_query(const void* arg) {
 
 int in_capacity(int tin, int tout, const InPlan& plan) {
   char key[128];
-  std::snprintf(key, sizeof key, "in|%d|%d|%d|%d|%d|%d|%d|%d|%d", tin, tout,
+  std::snprintf(key, sizeof key, "in|%d|%d|%d|%d|%d|%d|%d|%d|%d|%d", tin, tout,
                 static_cast<int>(plan.path), plan.vec ? 1 : 0, plan.threads, plan.nv, plan.ns,
-                plan.group, plan.cluster);
+                plan.group, plan.cluster, plan.packed ? 1 : 0);
   InQuery q{tin, tout, plan};
   return occupancy_cached(key, in_query, &q);
 }
@@ -284,12 +284,22 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
       plan.nv = std::atoi(u) == kStreamUnrollFew ? kStreamUnrollFew : kStreamUnroll;
   }
 
+  // bf16 slices spread over clusters of more than 8 CTAs take the packed pair
+  // arithmetic (shapes with 8 register and 8 staged slots); FNORM_NO_PACK=1
+  // keeps the scalar loops
+  auto set_packed = [&] {
+    plan.packed = plan.path == InPath::kSplit && tin == 1 && plan.cluster > 8 && plan.nv == 8 &&
+                  plan.ns == 8 && (plan.threads == 256 || plan.threads == 512 ||
+                                   plan.threads == 1024) && !env("FNORM_NO_PACK");
+  };
+  set_packed();
   int cap = in_capacity(tin, tout, plan);
   if (cap <= 0 && plan.path == InPath::kSplit && plan.cluster > 8 && !env("FNORM_FORCE_PATH") &&
       !env("FNORM_SPLIT_SHAPE")) {
     // 16-CTA clusters not available: twice the chunk per CTA, half the CTAs
     plan.threads *= 2;
     plan.cluster = static_cast<int>((slots + plan.threads * 16 - 1) / (plan.threads * 16));
+    set_packed();
     cap = in_capacity(tin, tout, plan);
   }
   if (cap <= 0 && plan.path != InPath::kGroup && plan.cluster > 8 && !env("FNORM_FORCE_PATH")) {
@@ -298,6 +308,7 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
     plan.threads = kStreamThreads;
     plan.nv = kStreamUnroll;
     plan.cluster = 8;
+    set_packed();
     cap = in_capacity(tin, tout, plan);
   }
   if (cap <= 0) return FNORM_ERR_UNSUPPORTED;
@@ -313,10 +324,10 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
   if (env("FNORM_DEBUG_PLAN"))
     std::fprintf(stderr,
                  "fnorm_instancenorm plan: path=%d vec=%d threads=%d nv=%d ns=%d group=%d "
-                 "cluster=%d grid=%d capacity=%d NC=%lld S=%lld\n",
+                 "cluster=%d packed=%d grid=%d capacity=%d NC=%lld S=%lld\n",
                  static_cast<int>(plan.path), plan.vec ? 1 : 0, plan.threads, plan.nv, plan.ns,
                  plan.group,
-                 plan.cluster, plan.grid, cap, static_cast<long long>(NC),
+                 plan.cluster, plan.packed ? 1 : 0, plan.grid, cap, static_cast<long long>(NC),
                  static_cast<long long>(S));
   *out = plan;
   return FNORM_OK;

@@ -44,6 +44,7 @@ struct InPlan {
   int group;     // lanes per slice (group path)
   int cluster;   // CTAs per slice (resident / stream); 1 = no cluster
   int grid;      // CTAs to launch (0: the launcher sizes the persistent grid)
+  bool packed;   // split path, bf16 input, cluster > 8: packed pair arithmetic
 };
 
 // Launch plans the kernel files provide, listed so the dispatcher can choose

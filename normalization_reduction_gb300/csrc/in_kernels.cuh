@@ -501,11 +501,64 @@ __device__ __forceinline__ float2 cluster_exchange(const Stat& cta, float4 (*slo
   return *fin;
 }
 
-template <class Tin, class Tout, int THREADS, int NR, int NS>
+// Packed pair arithmetic for bf16 inputs: the two values of one 32-bit word of
+// a slot (elements 2i, 2i+1) widened into an fp32 pair and processed by one
+// f32x2 instruction (__fadd2_rn / __ffma2_rn). With accumulator j & 3 held as
+// component (j & 1) of pair 01 (words 0, 2) or 23 (words 1, 3), every
+// accumulator sees the same operations in the same order and rounding as the
+// scalar loops (x - a is x + (-a), which is exact), so the results are
+// bit-identical; the floating-point instructions halve, which matters because
+// bf16 slices are issue-bound (twice the values per byte of fp32).
+__device__ __forceinline__ float2 bf16_pair_opaque(unsigned w) {
+  unsigned lo, hi;
+  asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w));
+  asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w));
+  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+
+// s += v - x0 (nx0 = (-x0, -x0))
+__device__ __forceinline__ void bf16_acc_shift(const uint4& v, float2 nx0, float2& s01, float2& s23) {
+  s01 = __fadd2_rn(s01, __fadd2_rn(bf16_pair_opaque(v.x), nx0));
+  s23 = __fadd2_rn(s23, __fadd2_rn(bf16_pair_opaque(v.y), nx0));
+  s01 = __fadd2_rn(s01, __fadd2_rn(bf16_pair_opaque(v.z), nx0));
+  s23 = __fadd2_rn(s23, __fadd2_rn(bf16_pair_opaque(v.w), nx0));
+}
+
+// q += (v - mean)^2 (nm = (-mean, -mean))
+__device__ __forceinline__ void bf16_acc_sq(const uint4& v, float2 nm, float2& q01, float2& q23) {
+  float2 d = __fadd2_rn(bf16_pair_opaque(v.x), nm);
+  q01 = __ffma2_rn(d, d, q01);
+  d = __fadd2_rn(bf16_pair_opaque(v.y), nm);
+  q23 = __ffma2_rn(d, d, q23);
+  d = __fadd2_rn(bf16_pair_opaque(v.z), nm);
+  q01 = __ffma2_rn(d, d, q01);
+  d = __fadd2_rn(bf16_pair_opaque(v.w), nm);
+  q23 = __ffma2_rn(d, d, q23);
+}
+
+// o = (v - mean) * a + b
+__device__ __forceinline__ void bf16_norm(const uint4& v, float2 nm, float2 a2, float2 b2, float (&o)[8]) {
+  const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 r = __ffma2_rn(__fadd2_rn(bf16_pair_opaque(w[i]), nm), a2, b2);
+    o[2 * i] = r.x;
+    o[2 * i + 1] = r.y;
+  }
+}
+
+template <class Tin, class Tout, int THREADS, int NR, int NS, bool PACK>
 __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     in_split_kernel(const InParams p) {
   using E = Elem<Tin>;
   constexpr int W = E::W;
+  // bf16 input, PACK: packed pair arithmetic (bf16_acc_*, bf16_norm). The
+  // plan sets PACK for slices spread over clusters of more than 8 CTAs, where
+  // a slice's arithmetic sits between the arrival of its data and the cluster
+  // exchange (bf16 S = 2^20, 16-CTA clusters: 4793 -> 5013 GB/s); with 8, 4
+  // and 1 CTAs per slice it measured equal or up to 2 % slower, and those
+  // keep the scalar loops.
+  constexpr bool kPackedBf16 = PACK && W == 8;
   extern __shared__ __align__(128) uint4 stage[];   // [NS][THREADS] slots
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ __align__(16) float4 slots[2][kMaxCluster];
@@ -565,7 +618,28 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     }
     // exact two-pass over this thread's values, shifted by its first value
     Stat st = stat_empty();
-    if (nvalid > 0) {
+    if (kPackedBf16 && nvalid > 0) {
+      const float x0 = E::get_opaque(ns_valid > 0 ? stage[tid] : r[0], 0);
+      const float2 nx0 = make_float2(-x0, -x0);
+      float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < NS; ++k)
+        if (k < ns_valid) bf16_acc_shift(stage[k * THREADS + tid], nx0, s01, s23);
+#pragma unroll
+      for (int k = 0; k < NR; ++k)
+        if (k < nr_valid) bf16_acc_shift(r[k], nx0, s01, s23);
+      const float n = static_cast<float>(nvalid);
+      const float mean = x0 + ((s01.x + s01.y) + (s23.x + s23.y)) / n;
+      const float2 nm = make_float2(-mean, -mean);
+      float2 q01 = make_float2(0.f, 0.f), q23 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < NS; ++k)
+        if (k < ns_valid) bf16_acc_sq(stage[k * THREADS + tid], nm, q01, q23);
+#pragma unroll
+      for (int k = 0; k < NR; ++k)
+        if (k < nr_valid) bf16_acc_sq(r[k], nm, q01, q23);
+      st = Stat{n, mean, (q01.x + q01.y) + (q23.x + q23.y)};
+    } else if (nvalid > 0) {
       const float x0 = E::get_opaque(ns_valid > 0 ? stage[tid] : r[0], 0);
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -624,8 +698,12 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
       if (k < ns_valid) {
         const uint4 v = stage[k * THREADS + tid];
         float o[W];
+        if constexpr (kPackedBf16) {
+          bf16_norm(v, make_float2(-mr.x, -mr.x), make_float2(ab.x, ab.x), make_float2(ab.y, ab.y), o);
+        } else {
 #pragma unroll
-        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(v, j) - mr.x, ab.x, ab.y);
+          for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(v, j) - mr.x, ab.x, ab.y);
+        }
         VecStore<Tout, W>::run(yq + (base + int64_t(k) * THREADS + tid) * W, o);
       }
     }
@@ -642,8 +720,12 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     for (int k = 0; k < NR; ++k) {
       if (k < nr_valid) {
         float o[W];
+        if constexpr (kPackedBf16) {
+          bf16_norm(r[k], make_float2(-mr.x, -mr.x), make_float2(ab.x, ab.x), make_float2(ab.y, ab.y), o);
+        } else {
 #pragma unroll
-        for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(r[k], j) - mr.x, ab.x, ab.y);
+          for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(r[k], j) - mr.x, ab.x, ab.y);
+        }
         VecStore<Tout, W>::run(yq + (rbase + int64_t(k) * THREADS) * W, o);
       }
     }
@@ -760,9 +842,19 @@ static void* pick_kernel(const InPlan& plan) {
       return nullptr;
     case InPath::kSplit:
       if (!VEC) return nullptr;
+      if (plan.packed) {
+        if constexpr (Elem<Tin>::W == 8) {
+#define FNORM_SPLIT_P(T, R, SM)                                      \
+  if (plan.threads == T && plan.nv == R && plan.ns == SM)            \
+    return reinterpret_cast<void*>(&in_split_kernel<Tin, Tout, T, R, SM, true>);
+          FNORM_SPLIT_P(256, 8, 8) FNORM_SPLIT_P(512, 8, 8) FNORM_SPLIT_P(1024, 8, 8)
+#undef FNORM_SPLIT_P
+        }
+        return nullptr;
+      }
 #define FNORM_SPLIT(T, R, SM)                                        \
   if (plan.threads == T && plan.nv == R && plan.ns == SM)            \
-    return reinterpret_cast<void*>(&in_split_kernel<Tin, Tout, T, R, SM>);
+    return reinterpret_cast<void*>(&in_split_kernel<Tin, Tout, T, R, SM, false>);
       FNORM_SPLIT(128, 8, 8) FNORM_SPLIT(256, 8, 8) FNORM_SPLIT(512, 8, 8) FNORM_SPLIT(1024, 8, 8)
       FNORM_SPLIT(64, 8, 0) FNORM_SPLIT(128, 8, 0) FNORM_SPLIT(256, 8, 0) FNORM_SPLIT(512, 8, 0)
       FNORM_SPLIT(1024, 8, 0)

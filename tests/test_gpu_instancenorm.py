@@ -250,3 +250,28 @@ def test_few_long_slices(orc, shape, dt):
     y, _, _ = run_in(x, dt)
     ref, _, _ = oracle_in(orc, x)
     assert_close(to_f64(y), ref, dt, f"few long slices {shape}")
+
+
+PACKED_CASES = [(3, 1 << 20, None), (2, 1047776, None), (3, 300000, "split:256:8:8:12"),
+                (2, 600000, "split:512:8:8:10"), (4, 262144, None)]
+
+
+@pytest.mark.parametrize("NC,S,path", PACKED_CASES,
+                         ids=[f"{n}x{s}-{p or 'default'}" for n, s, p in PACKED_CASES])
+@pytest.mark.parametrize("tout", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_bf16_packed_matches_scalar(orc, monkeypatch, NC, S, path, tout):
+    """bf16 slices spread over clusters of more than 8 CTAs take packed pair
+    arithmetic (two fp32 lanes per instruction). It performs the scalar loops'
+    operations in their order and rounding, so outputs and statistics must
+    equal those of the scalar loops (FNORM_NO_PACK=1) bit for bit, and match
+    the oracle. The last case (8-CTA clusters) runs the scalar loops both
+    times."""
+    if path:
+        monkeypatch.setenv("FNORM_FORCE_PATH", path)
+    x = make_x(NC, S, torch.bfloat16, 5150 + S % 997)
+    y1, m1, r1 = run_in(x, out_dtype=tout, stats=True)
+    monkeypatch.setenv("FNORM_NO_PACK", "1")
+    y2, m2, r2 = run_in(x, out_dtype=tout, stats=True)
+    assert torch.equal(y1, y2) and torch.equal(m1, m2) and torch.equal(r1, r2)
+    ref, _, _ = oracle_in(orc, x)
+    assert_close(to_f64(y1), ref, tout, f"packed {NC}x{S} {path}")
