@@ -503,12 +503,9 @@ __device__ __forceinline__ float2 cluster_exchange(const Stat& cta, float4 (*slo
 
 // Packed pair arithmetic for bf16 inputs: the two values of one 32-bit word of
 // a slot (elements 2i, 2i+1) widened into an fp32 pair and processed by one
-// f32x2 instruction (__fadd2_rn / __ffma2_rn). With accumulator j & 3 held as
-// component (j & 1) of pair 01 (words 0, 2) or 23 (words 1, 3), every
-// accumulator sees the same operations in the same order and rounding as the
-// scalar loops (x - a is x + (-a), which is exact), so the results are
-// bit-identical; the floating-point instructions halve, which matters because
-// bf16 slices are issue-bound (twice the values per byte of fp32).
+// f32x2 instruction (__fadd2_rn / __ffma2_rn), which halves the floating-point
+// instructions of slices that are issue-bound (a byte of bf16 holds twice the
+// values of fp32).
 __device__ __forceinline__ float2 bf16_pair_opaque(unsigned w) {
   unsigned lo, hi;
   asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w));
@@ -516,23 +513,24 @@ __device__ __forceinline__ float2 bf16_pair_opaque(unsigned w) {
   return make_float2(__uint_as_float(lo), __uint_as_float(hi));
 }
 
-// s += v - x0 (nx0 = (-x0, -x0))
-__device__ __forceinline__ void bf16_acc_shift(const uint4& v, float2 nx0, float2& s01, float2& s23) {
-  s01 = __fadd2_rn(s01, __fadd2_rn(bf16_pair_opaque(v.x), nx0));
-  s23 = __fadd2_rn(s23, __fadd2_rn(bf16_pair_opaque(v.y), nx0));
-  s01 = __fadd2_rn(s01, __fadd2_rn(bf16_pair_opaque(v.z), nx0));
-  s23 = __fadd2_rn(s23, __fadd2_rn(bf16_pair_opaque(v.w), nx0));
-}
-
-// q += (v - mean)^2 (nm = (-mean, -mean))
-__device__ __forceinline__ void bf16_acc_sq(const uint4& v, float2 nm, float2& q01, float2& q23) {
-  float2 d = __fadd2_rn(bf16_pair_opaque(v.x), nm);
+// Shifted sums of a thread's bf16 values in one pass: d = x - K (nk = (-K, -K),
+// K the thread's first value), s += d, q += d^2, as pairs (words 0, 2 into 01;
+// 1, 3 into 23). mean = K + S/n and M2 = Q - S^2/n follow; K is one of the
+// values, so (K - mean)^2 <= M2 and the cancellation is bounded by the
+// thread's count (at most 128 values in the kernels that use it).
+__device__ __forceinline__ void bf16_acc_onepass(const uint4& v, float2 nk, float2& s01, float2& s23,
+                                                 float2& q01, float2& q23) {
+  float2 d = __fadd2_rn(bf16_pair_opaque(v.x), nk);
+  s01 = __fadd2_rn(s01, d);
   q01 = __ffma2_rn(d, d, q01);
-  d = __fadd2_rn(bf16_pair_opaque(v.y), nm);
+  d = __fadd2_rn(bf16_pair_opaque(v.y), nk);
+  s23 = __fadd2_rn(s23, d);
   q23 = __ffma2_rn(d, d, q23);
-  d = __fadd2_rn(bf16_pair_opaque(v.z), nm);
+  d = __fadd2_rn(bf16_pair_opaque(v.z), nk);
+  s01 = __fadd2_rn(s01, d);
   q01 = __ffma2_rn(d, d, q01);
-  d = __fadd2_rn(bf16_pair_opaque(v.w), nm);
+  d = __fadd2_rn(bf16_pair_opaque(v.w), nk);
+  s23 = __fadd2_rn(s23, d);
   q23 = __ffma2_rn(d, d, q23);
 }
 
@@ -552,12 +550,13 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     in_split_kernel(const InParams p) {
   using E = Elem<Tin>;
   constexpr int W = E::W;
-  // bf16 input, PACK: packed pair arithmetic (bf16_acc_*, bf16_norm). The
+  // bf16 input, PACK: one pass of shifted sums for the statistics and the
+  // normalisation, both as packed pairs (bf16_acc_onepass, bf16_norm). The
   // plan sets PACK for slices spread over clusters of more than 8 CTAs, where
   // a slice's arithmetic sits between the arrival of its data and the cluster
-  // exchange (bf16 S = 2^20, 16-CTA clusters: 4793 -> 5013 GB/s); with 8, 4
-  // and 1 CTAs per slice it measured equal or up to 2 % slower, and those
-  // keep the scalar loops.
+  // exchange (bf16 S = 2^20, 16-CTA clusters: 5002 -> 5720 GB/s); with 8 or 1
+  // CTAs per slice the same code measured 0.5-4 % slower, and those keep the
+  // exact two-pass scalar loops.
   constexpr bool kPackedBf16 = PACK && W == 8;
   extern __shared__ __align__(128) uint4 stage[];   // [NS][THREADS] slots
   __shared__ Stat warp_part[THREADS / 32];
@@ -619,26 +618,19 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     // exact two-pass over this thread's values, shifted by its first value
     Stat st = stat_empty();
     if (kPackedBf16 && nvalid > 0) {
-      const float x0 = E::get_opaque(ns_valid > 0 ? stage[tid] : r[0], 0);
-      const float2 nx0 = make_float2(-x0, -x0);
-      float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
+      // one pass of shifted sums as pairs (bf16_acc_onepass)
+      const float K = E::get_opaque(ns_valid > 0 ? stage[tid] : r[0], 0);
+      const float2 nk = make_float2(-K, -K);
+      float2 s01 = make_float2(0.f, 0.f), s23 = s01, q01 = s01, q23 = s01;
 #pragma unroll
       for (int k = 0; k < NS; ++k)
-        if (k < ns_valid) bf16_acc_shift(stage[k * THREADS + tid], nx0, s01, s23);
+        if (k < ns_valid) bf16_acc_onepass(stage[k * THREADS + tid], nk, s01, s23, q01, q23);
 #pragma unroll
       for (int k = 0; k < NR; ++k)
-        if (k < nr_valid) bf16_acc_shift(r[k], nx0, s01, s23);
+        if (k < nr_valid) bf16_acc_onepass(r[k], nk, s01, s23, q01, q23);
       const float n = static_cast<float>(nvalid);
-      const float mean = x0 + ((s01.x + s01.y) + (s23.x + s23.y)) / n;
-      const float2 nm = make_float2(-mean, -mean);
-      float2 q01 = make_float2(0.f, 0.f), q23 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < NS; ++k)
-        if (k < ns_valid) bf16_acc_sq(stage[k * THREADS + tid], nm, q01, q23);
-#pragma unroll
-      for (int k = 0; k < NR; ++k)
-        if (k < nr_valid) bf16_acc_sq(r[k], nm, q01, q23);
-      st = Stat{n, mean, (q01.x + q01.y) + (q23.x + q23.y)};
+      const float sd = (s01.x + s01.y) + (s23.x + s23.y), qd = (q01.x + q01.y) + (q23.x + q23.y);
+      st = Stat{n, K + sd / n, fmaxf(qd - sd * (sd / n), 0.f)};
     } else if (nvalid > 0) {
       const float x0 = E::get_opaque(ns_valid > 0 ? stage[tid] : r[0], 0);
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
