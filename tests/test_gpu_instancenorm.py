@@ -280,3 +280,25 @@ def test_bf16_packed_matches_scalar(orc, monkeypatch, NC, S, path, tout, dist):
         assert np.allclose(r.cpu().numpy()[:NC], 1 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)
     if S == 262144:
         assert torch.equal(y1, y2) and torch.equal(m1, m2) and torch.equal(r1, r2)
+
+
+@pytest.mark.parametrize("S,threads,chunk", [(1 << 20, 512, 8192), (1 << 19, 256, 4096)])
+def test_bf16_packed_outliers_at_thread_shifts(orc, S, threads, chunk):
+    """The packed form's one-pass sums are shifted by each thread's first value
+    (its first staged vector: vector r*chunk + t of CTA r's chunk, element 0).
+    An outlier there is their worst case: put one at every thread's shift, on
+    data with a large offset, and compare with the oracle (fp32 output)."""
+    NC = 2
+    g = torch.Generator().manual_seed(777 + S)
+    x = torch.randn(NC, S, generator=g) * 0.5 + 3.0
+    nvec = S // 8
+    for r in range((nvec + chunk - 1) // chunk):
+        for t in range(threads):
+            v = r * chunk + t
+            if v < nvec:
+                x[:, 8 * v] = 3.0 + (400.0 if t % 2 else -400.0)
+    x = x.to(torch.bfloat16).to(dev())
+    y, m, rs = run_in(x, out_dtype=torch.float32, stats=True)
+    ref, rmean, rvar = oracle_in(orc, x)
+    assert_close(to_f64(y), ref, torch.float32, f"thread-shift outliers S={S}")
+    assert np.allclose(rs.cpu().numpy()[:NC], 1 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)
