@@ -100,6 +100,50 @@ __device__ __forceinline__ Stat tile_stat(const uint4 (&r)[NV], int nvalid) {
   return Stat{n, mean, (q[0] + q[1]) + (q[2] + q[3])};
 }
 
+// Packed pair arithmetic for bf16 inputs: the two values of one 32-bit word of
+// a slot (elements 2i, 2i+1) widened into an fp32 pair and processed by one
+// f32x2 instruction (__fadd2_rn / __ffma2_rn), which halves the floating-point
+// instructions of slices that are issue-bound (a byte of bf16 holds twice the
+// values of fp32).
+__device__ __forceinline__ float2 bf16_pair_opaque(unsigned w) {
+  unsigned lo, hi;
+  asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w));
+  asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w));
+  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+
+// Shifted sums of a thread's bf16 values in one pass: d = x - K (nk = (-K, -K),
+// K the thread's first value), s += d, q += d^2, as pairs (words 0, 2 into 01;
+// 1, 3 into 23). mean = K + S/n and M2 = Q - S^2/n follow; K is one of the
+// values, so (K - mean)^2 <= M2 and the cancellation is bounded by the
+// thread's count (at most 128 values in the kernels that use it).
+__device__ __forceinline__ void bf16_acc_onepass(const uint4& v, float2 nk, float2& s01, float2& s23,
+                                                 float2& q01, float2& q23) {
+  float2 d = __fadd2_rn(bf16_pair_opaque(v.x), nk);
+  s01 = __fadd2_rn(s01, d);
+  q01 = __ffma2_rn(d, d, q01);
+  d = __fadd2_rn(bf16_pair_opaque(v.y), nk);
+  s23 = __fadd2_rn(s23, d);
+  q23 = __ffma2_rn(d, d, q23);
+  d = __fadd2_rn(bf16_pair_opaque(v.z), nk);
+  s01 = __fadd2_rn(s01, d);
+  q01 = __ffma2_rn(d, d, q01);
+  d = __fadd2_rn(bf16_pair_opaque(v.w), nk);
+  s23 = __fadd2_rn(s23, d);
+  q23 = __ffma2_rn(d, d, q23);
+}
+
+// o = (v - mean) * a + b
+__device__ __forceinline__ void bf16_norm(const uint4& v, float2 nm, float2 a2, float2 b2, float (&o)[8]) {
+  const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 r = __ffma2_rn(__fadd2_rn(bf16_pair_opaque(w[i]), nm), a2, b2);
+    o[2 * i] = r.x;
+    o[2 * i + 1] = r.y;
+  }
+}
+
 __device__ __forceinline__ int clamp_int(int64_t v, int lo, int hi) {
   return v < lo ? lo : (v > hi ? hi : static_cast<int>(v));
 }
@@ -499,50 +543,6 @@ __device__ __forceinline__ float2 cluster_exchange(const Stat& cta, float4 (*slo
   }
   __syncthreads();
   return *fin;
-}
-
-// Packed pair arithmetic for bf16 inputs: the two values of one 32-bit word of
-// a slot (elements 2i, 2i+1) widened into an fp32 pair and processed by one
-// f32x2 instruction (__fadd2_rn / __ffma2_rn), which halves the floating-point
-// instructions of slices that are issue-bound (a byte of bf16 holds twice the
-// values of fp32).
-__device__ __forceinline__ float2 bf16_pair_opaque(unsigned w) {
-  unsigned lo, hi;
-  asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w));
-  asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w));
-  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
-}
-
-// Shifted sums of a thread's bf16 values in one pass: d = x - K (nk = (-K, -K),
-// K the thread's first value), s += d, q += d^2, as pairs (words 0, 2 into 01;
-// 1, 3 into 23). mean = K + S/n and M2 = Q - S^2/n follow; K is one of the
-// values, so (K - mean)^2 <= M2 and the cancellation is bounded by the
-// thread's count (at most 128 values in the kernels that use it).
-__device__ __forceinline__ void bf16_acc_onepass(const uint4& v, float2 nk, float2& s01, float2& s23,
-                                                 float2& q01, float2& q23) {
-  float2 d = __fadd2_rn(bf16_pair_opaque(v.x), nk);
-  s01 = __fadd2_rn(s01, d);
-  q01 = __ffma2_rn(d, d, q01);
-  d = __fadd2_rn(bf16_pair_opaque(v.y), nk);
-  s23 = __fadd2_rn(s23, d);
-  q23 = __ffma2_rn(d, d, q23);
-  d = __fadd2_rn(bf16_pair_opaque(v.z), nk);
-  s01 = __fadd2_rn(s01, d);
-  q01 = __ffma2_rn(d, d, q01);
-  d = __fadd2_rn(bf16_pair_opaque(v.w), nk);
-  s23 = __fadd2_rn(s23, d);
-  q23 = __ffma2_rn(d, d, q23);
-}
-
-// o = (v - mean) * a + b
-__device__ __forceinline__ void bf16_norm(const uint4& v, float2 nm, float2 a2, float2 b2, float (&o)[8]) {
-  const unsigned w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 r = __ffma2_rn(__fadd2_rn(bf16_pair_opaque(w[i]), nm), a2, b2);
-    o[2 * i] = r.x;
-    o[2 * i + 1] = r.y;
-  }
 }
 
 template <class Tin, class Tout, int THREADS, int NR, int NS, bool PACK>
