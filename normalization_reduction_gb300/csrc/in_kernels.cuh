@@ -15,7 +15,11 @@
 //    the split form also slots in shared memory filled by a TMA bulk copy
 //    that is issued for the next slice while the current one is processed.
 //  * Per thread, an exact two-pass mean/M2 over its own values (shifted by its
-//    first value so a constant slice gives M2 = 0 and the exact mean), then
+//    first value so a constant slice gives M2 = 0 and the exact mean). bf16
+//    slices spread over clusters of more than 8 CTAs, which are issue-bound,
+//    instead take one pass of sums shifted by the thread's first value (at
+//    most 128 values, so the cancellation stays bounded) and normalise, both
+//    as packed fp32 pairs. Then
 //    the Chan pairwise merge: warp shuffles -> shared memory across warps ->
 //    the CTAs of a thread-block cluster when one slice spans several CTAs (up
 //    to 16, i.e. 2 MiB of input per slice; partials pushed with st.async).
