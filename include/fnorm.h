@@ -82,6 +82,9 @@ typedef enum fnorm_dtype {
  * A slice is read from HBM once and written once whenever it fits in one
  * thread-block cluster (up to 2 MiB of input per slice); longer slices are
  * read twice (statistics pass, then normalisation pass).
+ * Statistics are accumulated in fp32 and merged in a fixed order: results are
+ * deterministic for a given call shape and agree with the exact definition to
+ * fp32 accuracy.
  */
 FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
                                 fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
@@ -124,6 +127,10 @@ FNORM_API fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const f
  * statistics, and the output pass re-reads it from L2 (the leading part of
  * each channel's range from shared memory), so HBM sees about one read of x
  * while the input fits in L2. Other shapes stream each slice twice.
+ * Rounding: the statistics are fp32 and the results agree with the exact
+ * definition to fp32 accuracy; without argmax the clamp is evaluated as an
+ * equivalent saturating multiply-add, so y may differ from the argmax call's
+ * y in the last bits. Results are deterministic for a given call shape.
  */
 FNORM_API fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
                                          int64_t N, int64_t C, int64_t S, float eps,
