@@ -2,7 +2,13 @@
 x once, write y once) and the fraction of the measured HBM peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--shape N,C,H,W] [--no-extra]
+                    [--workload NAME] [--shape N,C,H,W] [--no-extra] [--dry-run]
+
+``--gpus N`` runs one process per GPU: launched without torchrun, the script
+re-launches itself under ``torch.distributed.run`` with N processes; under a
+launcher, WORLD_SIZE must equal N. ``--dry-run`` prints that plan and exits.
+At least 3 warm-up steps run; the line's ``warmup`` is the number used (and
+``warmup_requested`` the one asked for, when they differ).
 
 One step is one call of the hot path over one batch of the workload. The
 default workload is InstanceNorm2d forward, fp32, x[112,64,512,512] ~ N(0,1)
@@ -40,15 +46,16 @@ NOMINAL_HBM_GBS = 7900.0
 L2_BYTES = 126 * 1024 * 1024
 
 # DRAM bytes (read + write) per launch of each workload's dominant kernel from
-# one ncu capture (profiles/*.md); None until measured for the current kernel.
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum); None until
+# measured for the current kernel.
 NCU_TRAFFIC = {
-    # profiles/in_split_kernel__instancenorm_fp32_112x64x512x512.md: 1.073823 GB read +
-    # 1.018198 GB written for 1024 slices, scaled by 7 to the 7168-slice launch
+    # the split InstanceNorm kernel: 1.073823 GB read + 1.018198 GB written for
+    # 1024 slices (x[16,64,512,512]), scaled by 7 to the 7168-slice launch
     "instancenorm2d_fp32_112x64x512x512": 14644147000,
-    # profiles/bn_eval_staged_kernel__batchnorm_eval_fp32_128x64x126x126.md (full size)
+    # the eval BatchNorm kernel at full size
     "batchnorm2d_eval_fp32_128x64x126x126": 984366848,
-    # profiles/bn_kernels__batchnorm_train_fp32_128x64x126x126.md: both launches of a step
-    # (caches flushed between them by ncu, so without the apply pass's L2 reuse)
+    # both launches of a training BatchNorm step (caches flushed between them
+    # by ncu, so without the apply pass's L2 reuse)
     "batchnorm2d_train_fp32_128x64x126x126": 1506137856,
 }
 
@@ -204,6 +211,42 @@ class Sweep(Workload):
                               1e-5, None, None, stream)
 
 
+class Floor(Workload):
+    """Reference floors for the roofline (not the library): a plain read of
+    BYTES bytes (torch's sum over an fp32 tensor) or a copy (torch's copy_),
+    rotating over input copies of at least 4x L2 in total when BYTES is below
+    that, so every step reads HBM. The epilogue's workload reads 103 MB and
+    writes 6.5 MB; its floor is about a 103 MB read."""
+    kernel = "torch reference (not libfnorm)"
+    launches = 0
+    graph = True
+
+    def __init__(self, dev, kind, nbytes):
+        self.kind = kind
+        self.name = f"floor_{kind}_{nbytes}B"
+        n = max(1, nbytes // 4)
+        copies = max(1, -(-4 * L2_BYTES // (n * 4)))
+        self.xs = [torch.ones(n, device=dev) for _ in range(copies)]
+        self.ys = [torch.empty(n, device=dev) for _ in range(copies)] if kind == "copy" else []
+        self.out = torch.empty((), device=dev)
+        self.n = n
+        self.i = 0
+
+    def bytes_per_step(self):
+        return self.n * 4 * (2 if self.kind == "copy" else 1)
+
+    def l2_note(self):
+        return f"{len(self.xs)} rotating copies (>= 4x L2 in total)"
+
+    def step(self, stream):
+        k = self.i % len(self.xs)
+        self.i += 1
+        if self.kind == "copy":
+            self.ys[k].copy_(self.xs[k])
+        else:
+            torch.sum(self.xs[k], dim=0, out=self.out)
+
+
 # ------------------------------------------------------------------ timing
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
@@ -289,6 +332,9 @@ def make_workload(args, dev) -> Workload:
         return InstanceNormAffine(dev, shape or inputs.SHAPE_LARGE)
     if args.workload == "bn_eval":
         return BatchNormEval(dev)
+    if args.workload.startswith("floor_read:") or args.workload.startswith("floor_copy:"):
+        kind, nbytes = args.workload[len("floor_"):].split(":")
+        return Floor(dev, kind, int(nbytes))
     if args.workload.startswith("sweep:"):
         parts = args.workload.split(":")
         total = int(parts[2]) if len(parts) > 2 else inputs.SWEEP_TOTAL
@@ -501,6 +547,8 @@ def run_ours(args):
         "gpu_launches": wl.launches * args.steps,
         "clocks": clocks,
     }
+    if args.warmup_requested != args.warmup:
+        res["warmup_requested"] = args.warmup_requested
     res["dtype"] = wl.dtype
     if rank == 0 and not args.no_extra and isinstance(wl, InstanceNormLarge):
         res["e2e"] = e2e_instancenorm(wl, max(2, min(args.steps, 5)))
@@ -568,6 +616,8 @@ def run_reference(args):
                             "sample": f"{sample} of {NC} slices per step, float64 single-threaded"},
            "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
+    if args.warmup_requested != args.warmup:
+        res["warmup_requested"] = args.warmup_requested
     print(json.dumps(res), flush=True)
     del np
 
@@ -582,17 +632,33 @@ def main():
                     help="skip e2e, cpu baseline and the other workloads")
     ap.add_argument("--workload", default="in_large",
                     help="in_large | in_affine | epilogue | batchnorm | bn_eval | sweep:S[:TOTAL] "
-                         "(S a power of 4, 256..4^10; TOTAL elements, default 2^30)")
+                         "(S a power of 4, 256..4^10; TOTAL elements, default 2^30) | "
+                         "floor_read:BYTES | floor_copy:BYTES (torch reference floors)")
     ap.add_argument("--shape", default=None,
                     help="N,C,H,W for in_large (e.g. a smaller case for ncu)")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="print how the run would start (one line of JSON) and exit")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
+    plan = dist.launch_plan(args.gpus, os.environ, sys.argv[1:], os.path.abspath(__file__),
+                            sys.executable)
+    if args.dry_run:
+        print(json.dumps(plan), flush=True)
+        return 0 if plan["action"] != "error" else 2
+    if plan["action"] == "error":
+        print(f"bench.py: {plan['why']}", file=sys.stderr, flush=True)
+        return 2
+    if plan["action"] == "relaunch":
+        # one process per GPU under torch.distributed.run; rank 0 prints the line
+        return subprocess.run(plan["cmd"]).returncode
+    # at least 3 untimed warm-up steps; the line reports the number used
+    args.warmup_requested = args.warmup
+    args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -28,7 +28,12 @@
  *  - Statistics: the mean and the biased variance (divide by the element
  *    count) over each slice, combined across threads, CTAs and clusters with
  *    the Chan/Welford pairwise update; normalisation is
- *    (x - mean) * rsqrt(var + eps) computed in fp32.
+ *    (x - mean) * rsqrt(var + eps) computed in fp32. Element counts inside
+ *    the merges are fp32 values, exact up to 2^24 per merged part; above
+ *    that (a slice or BatchNorm channel of more than 16,777,216 values that
+ *    is not a multiple of the rounding step) a count carries a relative
+ *    rounding error of at most 2^-24, which moves the merge weights and the
+ *    variance by the same relative amount -- far below fp32 output accuracy.
  *  - Fast paths need x and y 16-byte aligned and the slice length a multiple
  *    of one 16-byte vector; other (element-aligned) inputs take a scalar-load
  *    path with the same results. Pointers not aligned to their element size
@@ -284,6 +289,29 @@ FNORM_API fnorm_status fnorm_get_last_error(void);
 
 /* Library version: major*10000 + minor*100 + patch. */
 FNORM_API int fnorm_version(void);
+
+/*
+ * Tuning and testing (not needed in normal use).
+ *
+ * The library reads its tuning switches -- environment variables named
+ * FNORM_* that force a kernel path or launch shape for experiments and tests
+ * (FNORM_FORCE_PATH, FNORM_SPLIT_SHAPE, FNORM_EPI_CLUSTER, FNORM_BN_SPLIT and
+ * the others listed with the library's documentation) -- once per process, at
+ * the first call that plans a launch. fnorm_tuning_reload() reads them again
+ * (after the process changed its environment); it must not run concurrently
+ * with any other libfnorm call.
+ *
+ * fnorm_debug_force_timeout(1) makes one CTA of every later launch that has a
+ * bounded-wait test hook (the epilogue range kernels, the split InstanceNorm
+ * kernel, the staged and resident BatchNorm kernels) wait, after its last
+ * cluster barrier, on a barrier that nothing completes: the wait expires
+ * after its 1 s limit, the kernel records FNORM_ERR_TIMEOUT in the device
+ * error word (fnorm_get_last_error) and returns, and the results are still
+ * written. fnorm_debug_force_timeout(0) turns it off (the default). It exists
+ * to test the failure path; no environment variable enables it.
+ */
+FNORM_API void fnorm_tuning_reload(void);
+FNORM_API void fnorm_debug_force_timeout(int on);
 
 #ifdef __cplusplus
 }

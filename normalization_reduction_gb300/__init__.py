@@ -24,6 +24,7 @@ __all__ = [
     "fnorm_batchnorm_workspace_size", "fnorm_batchnorm_eval",
     "fnorm_batchnorm_train", "fnorm_batchnorm_train_noalloc", "fnorm_batchnorm_local_stats",
     "fnorm_batchnorm_apply_stats", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
+    "fnorm_tuning_reload", "fnorm_debug_force_timeout",
     "instance_norm", "instance_norm_epilogue", "batch_norm_train", "batch_norm_eval",
 ]
 
@@ -74,6 +75,8 @@ _SIGNATURES = {
     "fnorm_status_string": ([_int], ctypes.c_char_p),
     "fnorm_get_last_error": ([], _int),
     "fnorm_version": ([], _int),
+    "fnorm_tuning_reload": ([], None),
+    "fnorm_debug_force_timeout": ([_int], None),
 }
 
 
@@ -198,6 +201,18 @@ def fnorm_get_last_error() -> Status:
 
 def fnorm_version() -> int:
     return int(lib().fnorm_version())
+
+
+def fnorm_tuning_reload() -> None:
+    """Re-reads the FNORM_* tuning switches from the environment (tests and
+    experiments; the library reads them once per process otherwise)."""
+    lib().fnorm_tuning_reload()
+
+
+def fnorm_debug_force_timeout(on: bool) -> None:
+    """Test hook: later launches with a bounded-wait hook make one CTA's wait
+    expire (FNORM_ERR_TIMEOUT in the error word); False turns it off."""
+    lib().fnorm_debug_force_timeout(1 if on else 0)
 
 
 # ---------------------------------------------------------------- torch helpers

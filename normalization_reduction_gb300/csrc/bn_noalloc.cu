@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/fnorm.h"
+#include "fnorm_internal.h"
 
 namespace {
 
@@ -55,13 +56,16 @@ extern "C" FNORM_API fnorm_status fnorm_batchnorm_train_noalloc(
     const float* x, float* y, const float* gamma, const float* beta, float scale,
     float* running_mean, float* running_var, float momentum, float eps, float* save_mean,
     float* save_rstd, int64_t N, int64_t C, int64_t S, fnorm_stream_t stream) {
-  // Shapes whose partial statistics do not fit the static scratch are refused
-  // before anything touches the GPU.
-  if (N > 0 && C > 0 && S > 0 &&
-      fnorm_batchnorm_workspace_size(N, C, S) > kNoallocScratchBytes)
+  // The arguments are checked exactly as fnorm_batchnorm_train checks them
+  // (same errors for the same mistakes); then shapes whose partial statistics
+  // do not fit the static scratch are refused, before anything touches the GPU.
+  int64_t total = 0;
+  const fnorm_status st =
+      fnorm::bn_train_check(x, y, gamma, beta, scale, running_mean, running_var, momentum, eps,
+                            save_mean, save_rstd, N, C, S, &total);
+  if (st != FNORM_OK || total == 0) return st;
+  if (fnorm_batchnorm_workspace_size(N, C, S) > kNoallocScratchBytes)
     return FNORM_ERR_UNSUPPORTED;
-  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
-  if (N == 0 || C == 0 || S == 0) return FNORM_OK;
   void* scratch = scratch_address();
   if (!scratch) return FNORM_ERR_CUDA;
   // The same validation and kernels as fnorm_batchnorm_train, with the static

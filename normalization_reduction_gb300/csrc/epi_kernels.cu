@@ -26,10 +26,6 @@
 //    shape, 103 MB, fits in L2), and writes max_c z_c (+ argmax; without the
 //    index the clamp is a saturating FMA and channels go in pairs through a
 //    three-input max).
-//  * epi_range_kernel (FNORM_EPI_STAGED=1): the range is staged in shared
-//    memory by TMA bulk copies, double-buffered across samples.
-//  * epi_ring_kernel (FNORM_EPI_RING=1): a producer warp streams the range
-//    through a TMA ring twice (statistics, then outputs).
 //  * epi_stream_kernel (inputs that are not 16-byte aligned or too wide):
 //    one cluster per sample, CTAs owning whole channels, each slice read twice
 //    with element-wise loads.
@@ -39,33 +35,10 @@
 
 namespace fnorm {
 
-// TMA ring form (below): stages in flight per CTA, consumer threads, channels
-// per consumer warp.
-constexpr int kEpiStages = 3;
-constexpr int kEpiRingCons = kEpiRingThreads - 32;   // 8 consumer warps
-constexpr int kEpiRingCpw = kEpiRingMaxC / (kEpiRingCons / 32);
-
-static __host__ __device__ __forceinline__ size_t align128(size_t v) {
-  return (v + 127) & ~size_t(127);
-}
-
-// Shared memory of the range kernel: two staging buffers of x [C][per]
-// float4, channel coefficients [C], partial slots [2][C][cluster].
-size_t epi_range_smem(int64_t C, int64_t per, int cluster) {
-  return 2 * align128(static_cast<size_t>(C) * per * 16) + static_cast<size_t>(C) * 16 +
-         2 * static_cast<size_t>(C) * cluster * 16;
-}
-
 size_t epi_range_l2_smem(int64_t C, int cluster, int keep) {
   return static_cast<size_t>(C) * 16 + 2 * static_cast<size_t>(C) * cluster * 16 +
-         static_cast<size_t>(C) * keep * 16;
+         static_cast<size_t>(C) * keep * 16 + ((static_cast<size_t>(C) * 4 + 15) & ~size_t(15));
 }
-
-size_t epi_ring_smem(int64_t C, int ring_t, int cluster) {
-  return static_cast<size_t>(kEpiStages) * C * ring_t * 16 + static_cast<size_t>(C) * 16 +
-         2 * static_cast<size_t>(C) * cluster * 16;
-}
-
 
 size_t epi_stream_smem(int64_t C, int cluster) {
   return static_cast<size_t>(C) * 16 + static_cast<size_t>((C + cluster - 1) / cluster) * 16;
@@ -104,166 +77,9 @@ __device__ __forceinline__ float epi_zc(float v, const float4& k) {
   return fminf(fmaxf(fmaf(v, k.x, k.y), k.z), k.w);
 }
 
-// Range kernel: cluster per sample, CTA r staging positions [r*per, ...) of all
-// C channels, double-buffered: while sample n is reduced and written, the
-// CTA's staging of sample n + 2*clusters is already in flight.
-template <int THREADS, bool WANT_ARG>
-__global__ void __launch_bounds__(THREADS) epi_range_kernel(const EpiParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t sbar[2];
-  __shared__ __align__(8) uint64_t xbar[2];
-  __shared__ __align__(8) uint64_t dbg_bar;
-  constexpr int NWARP = THREADS / 32;
-
-  const int64_t S = p.S;
-  const int C = static_cast<int>(p.C);
-  const int64_t per = p.per;                 // position vectors (of 4) per CTA
-  const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
-  const unsigned cid = cluster_id_x(), ncl = ncluster_x();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t stage_bytes = align128(size_t(C) * per * 16);
-  uint4* stage0 = reinterpret_cast<uint4*>(smem_raw);                       // [2][C][per]
-  float4* coef = reinterpret_cast<float4*>(smem_raw + 2 * stage_bytes);     // [C]
-  float4* slots = coef + C;                                                  // [2][C][csize]
-  const int64_t nv4 = S / 4;
-  const int64_t v0 = per * crank;
-  const int64_t vr = v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0;   // vectors owned
-  const unsigned seg_bytes = static_cast<unsigned>(vr * 16);
-
-  if (tid == 0) {
-    mbar_init(&sbar[0], 1);
-    mbar_init(&sbar[1], 1);
-    mbar_init(&xbar[0], 1);
-    mbar_init(&xbar[1], 1);
-    mbar_init(&dbg_bar, 1);
-    fence_mbar_init();
-  }
-  if (csize > 1) cluster_sync();   // peers' barriers exist before anyone signals them
-  else __syncthreads();
-  pdl_wait();
-
-  auto stage_of = [&](int b) { return reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(stage0) + b * stage_bytes); };
-  // One thread stages sample n into buffer b: C bulk copies, one barrier.
-  auto issue = [&](int64_t n, int b) {
-    mbar_arrive_expect_tx(&sbar[b], seg_bytes * static_cast<unsigned>(C));
-    uint4* st = stage_of(b);
-    for (int c = 0; c < C; ++c)
-      tma_bulk_g2s(st + int64_t(c) * per, p.x + (n * C + c) * S + v0 * 4, seg_bytes, &sbar[b]);
-  };
-  if (seg_bytes > 0 && tid == 0) {
-    if (cid < p.N) issue(cid, 0);
-    if (cid + ncl < p.N) issue(cid + ncl, 1);
-  }
-
-  bool failed = false, xfailed = false;
-  int it = 0;
-  for (int64_t n = cid; n < p.N; n += ncl, ++it) {
-    const int b = it & 1;
-    const unsigned use_parity = (static_cast<unsigned>(it) >> 1) & 1u;   // k-th use of buffer b
-    const uint4* xs = stage_of(b);
-    if (seg_bytes > 0 && !failed) {
-      bool ok = true;
-      if (warp == 0) ok = mbar_wait_bounded(&sbar[b], use_parity, p.err);
-      failed = __syncthreads_or(!ok) != 0;
-      // the waiting warp observed the completed copies; the others now observe
-      // the same completed phase without spinning
-      if (!failed && warp != 0) mbar_wait_bounded(&sbar[b], use_parity, p.err);
-    }
-    float4* sl = slots + size_t(b) * C * csize;
-    if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
-    // per-channel partial statistics over this CTA's range, one warp per channel
-    for (int c = warp; c < C; c += NWARP) {
-      const uint4* xc = xs + int64_t(c) * per;
-      Stat acc = stat_empty();
-      for (int64_t i = lane; i < vr; i += 32 * 4) {
-        uint4 r[4];
-        int nvalid = 0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const bool v = i + u * 32 < vr;
-          r[u] = v ? xc[i + u * 32] : make_uint4(0, 0, 0, 0);
-          nvalid += v ? 4 : 0;
-        }
-        acc = chan_merge(acc, tile_stat<float, 4>(r, nvalid));
-      }
-      acc = warp_merge<32>(acc);
-      const float4 v = make_float4(__shfl_sync(kFullMask, acc.n, 0), __shfl_sync(kFullMask, acc.mean, 0),
-                                   __shfl_sync(kFullMask, acc.m2, 0), 0.f);
-      // lane r pushes the partial to cluster rank r
-      for (unsigned rr = lane; rr < csize; rr += 32)
-        st_async_v4(&sl[size_t(c) * csize + crank], &xbar[b], rr, v);
-    }
-    // all partials of every channel: merge in rank order (one warp waits)
-    __syncthreads();
-    {
-      bool ok = true;
-      if (warp == 0 && !xfailed) ok = mbar_wait_bounded(&xbar[b], use_parity, p.err);
-      if (__syncthreads_or(!ok)) xfailed = true;
-    }
-    for (int c = warp; c < C; c += NWARP) {
-      Stat s = stat_empty();
-      if (lane < static_cast<int>(csize)) {
-        const float4 v = sl[size_t(c) * csize + lane];
-        s = Stat{v.x, v.y, v.z};
-      }
-      s = warp_merge<16>(s);
-      if (lane == 0) coef[c] = epi_out_coef(s, __ldg(p.m + c), p.eps, p.lo, p.hi);
-    }
-    __syncthreads();
-
-    // outputs of this CTA's positions, from the staged data
-    for (int64_t v = tid; v < vr; v += THREADS) {
-      float best[4];
-      int arg[4] = {0, 0, 0, 0};
-      {
-        const uint4 u = xs[v];
-        const float4 k = coef[0];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) best[j] = epi_zc(Elem<float>::get(u, j), k);
-      }
-      for (int c = 1; c < C; ++c) {
-        const uint4 u = xs[int64_t(c) * per + v];
-        const float4 k = coef[c];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float z = epi_zc(Elem<float>::get(u, j), k);
-          if (WANT_ARG) {
-            if (z > best[j]) {
-              best[j] = z;
-              arg[j] = c;
-            }
-          } else {
-            best[j] = fmaxf(best[j], z);
-          }
-        }
-      }
-      const int64_t pos = (v0 + v) * 4;
-      *reinterpret_cast<float4*>(p.y + n * S + pos) = make_float4(best[0], best[1], best[2], best[3]);
-      if (WANT_ARG) {
-        longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pos);
-        ao[0] = make_longlong2(arg[0], arg[1]);
-        ao[1] = make_longlong2(arg[2], arg[3]);
-      }
-    }
-    __syncthreads();   // buffer b and the coefficients consumed
-    const int64_t nn = n + 2 * int64_t(ncl);
-    if (seg_bytes > 0 && tid == 0 && nn < p.N && !failed) issue(nn, b);
-  }
-  pdl_trigger();
-  if (csize > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
-  if (failed && seg_bytes > 0) {   // let copies that may still be in flight land
-    mbar_wait_bounded(&sbar[0], 0, p.err);
-    mbar_wait_bounded(&sbar[1], 0, p.err);
-  }
-  // Test hook, after the last cluster barrier so no peer waits on this CTA:
-  // a wait on a barrier nothing completes must expire, record the timeout in
-  // the error word and return.
-  if (p.debug_timeout && cid == 0 && crank == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
-}
-
-// Range kernel, L2 form: the same decomposition (cluster per sample, CTA r
-// owning a range of positions of all channels, st.async exchange of the
-// per-channel partials) without staging. The statistics pass streams x from
+// Range kernel, L2 form: a cluster per sample, CTA r owning a range of
+// positions of all channels, st.async exchange of the per-channel partials.
+// The statistics pass streams x from
 // HBM with 128-bit loads, 8 per lane in flight, leaving it in L2; the output
 // pass reads the CTA's range again from L2 (4 channels' loads in flight per
 // thread). For the page's shape a sample is 806 KB and the whole input
@@ -402,6 +218,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
   // from the statistics pass for the output pass (fewer L2 re-reads)
   uint4* keep = reinterpret_cast<uint4*>(slots + 2 * C * csize);
   const int KS = KEEP >= 0 ? KEEP : p.keep;
+  float* mloc = reinterpret_cast<float*>(keep + static_cast<size_t>(C) * KS);   // [C]
   const int64_t nv4 = S / 4;
   const int64_t v0 = per * crank;
   const int vr = static_cast<int>(v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0);
@@ -419,6 +236,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
   // (the grid never exceeds the co-resident capacity); its CTAs take free
   // slots and wait in griddepcontrol.wait, which hides its launch.
   pdl_trigger();
+  for (int c = tid; c < C; c += THREADS) mloc[c] = __ldg(p.m + c);   // read after the barriers below
 
   bool xfailed = false;
   int it = 0;
@@ -499,16 +317,25 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
     if (warp == 0 && !xfailed)
       ok = mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(it) >> 1) & 1u, p.err);
     if (__syncthreads_or(!ok)) xfailed = true;
-    for (int c = warp; c < C; c += NWARP) {
-      Stat s = stat_empty();
-      if (lane < static_cast<int>(csize)) {
-        const float4 v = sl[size_t(c) * csize + lane];
-        s = Stat{v.x, v.y, v.z};
-      }
-      s = warp_merge<16>(s);
-      if (lane == 0) {
-        const float4 k = epi_out_coef(s, __ldg(p.m + c), p.eps, p.lo, p.hi);
-        coef[c] = WANT_ARG ? k : epi_sat_coef(k);
+    // Channel coefficients: segments of W lanes (W = csize rounded up to a
+    // power of two) each merge one channel's csize partials in a fixed tree
+    // (the same bits in every CTA), so a warp does 32/W channels at once.
+    {
+      const int W = csize <= 2 ? 2 : csize <= 4 ? 4 : csize <= 8 ? 8 : 16;
+      const int per_warp = 32 / W, seg = lane / W, r = lane - seg * W;
+      for (int c0 = warp * per_warp; c0 < C; c0 += NWARP * per_warp) {
+        const int c = c0 + seg;
+        Stat s = stat_empty();
+        if (c < C && r < static_cast<int>(csize)) {
+          const float4 v = sl[size_t(c) * csize + r];
+          s = Stat{v.x, v.y, v.z};
+        }
+        s = W == 2 ? warp_merge<2>(s) : W == 4 ? warp_merge<4>(s) : W == 8 ? warp_merge<8>(s)
+                                                                        : warp_merge<16>(s);
+        if (r == 0 && c < C) {
+          const float4 k = epi_out_coef(s, mloc[c], p.eps, p.lo, p.hi);
+          coef[c] = WANT_ARG ? k : epi_sat_coef(k);
+        }
       }
     }
     __syncthreads();
@@ -568,234 +395,6 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       }
     }
     __syncthreads();   // coefficients consumed before the next sample rewrites them
-  }
-  pdl_trigger();
-  if (csize > 1) cluster_sync();
-  // Test hook, after the last cluster barrier so no peer waits on this CTA:
-  // a wait on a barrier nothing completes must expire, record the timeout in
-  // the error word and return.
-  if (p.debug_timeout && cid == 0 && crank == 0) mbar_wait_bounded(&dbg_bar, 0, p.err);
-}
-
-__device__ __forceinline__ void named_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Range kernel, TMA ring form (FNORM_EPI_RING=1): the range decomposition of the
-// L2 form with all global reads done by the TMA engine. Per CTA, one producer
-// warp streams the CTA's position range of all C channels through a ring of
-// kEpiStages shared-memory stages (C bulk copies per stage, full/empty
-// mbarriers), twice per sample: pass 1 (from HBM) feeds the statistics, pass 2
-// (the same bytes again, mostly from L2) feeds the outputs. Eight consumer
-// warps compute from shared memory. The producer runs ahead of the consumers
-// by up to kEpiStages stages -- into pass 2 while the cluster exchange of the
-// statistics is still in flight, and into the next sample -- so each SM keeps
-// tens of KB of loads in flight at all times without spending registers.
-//   stage = C x T position vectors (16 B), T = ring_t (runtime, <= 256)
-//   pass 1: channel c is reduced by consumer warp c % 8, lanes over vectors;
-//           per-lane Chan accumulators (up to kEpiRingCpw channels per warp)
-//   pass 2: TPV = 256/T consumer threads per position vector, each over the
-//           channels c = h (mod TPV); (max, lowest index) combined by shuffles
-
-__device__ __forceinline__ void epi_combine(float& best, int& arg, float ob, int oa) {
-  if (ob > best || (ob == best && oa < arg)) {
-    best = ob;
-    arg = oa;
-  }
-}
-
-template <bool WANT_ARG>
-__global__ void __launch_bounds__(kEpiRingCons + 32, 2) epi_ring_kernel(const EpiParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kEpiStages];
-  __shared__ __align__(8) uint64_t empty_bar[kEpiStages];
-  __shared__ __align__(8) uint64_t xbar[2];
-  __shared__ __align__(8) uint64_t dbg_bar;
-  constexpr int NCW = kEpiRingCons / 32;    // consumer warps
-
-  const int64_t S = p.S;
-  const int C = static_cast<int>(p.C);
-  const int64_t per = p.per;
-  const int T = p.ring_t;
-  const unsigned crank = cluster_ctarank(), csize = cluster_nctarank();
-  const unsigned cid = cluster_id_x(), ncl = ncluster_x();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t stage_vecs = size_t(C) * T;
-  uint4* ring = reinterpret_cast<uint4*>(smem_raw);                                 // [stages][C][T]
-  float4* coef = reinterpret_cast<float4*>(ring + kEpiStages * stage_vecs);          // [C]
-  float4* slots = coef + C;                                                          // [2][C][csize]
-  const int64_t nv4 = S / 4;
-  const int64_t v0 = per * crank;
-  const int vr = static_cast<int>(v0 < nv4 ? (nv4 - v0 < per ? nv4 - v0 : per) : 0);
-  const int nch = (vr + T - 1) / T;                      // chunks per pass
-  const int K = cid < p.N ? static_cast<int>((p.N - 1 - cid) / ncl + 1) : 0;
-
-  if (tid == 0) {
-    for (int i = 0; i < kEpiStages; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], NCW);
-    }
-    mbar_init(&xbar[0], 1);
-    mbar_init(&xbar[1], 1);
-    mbar_init(&dbg_bar, 1);
-    fence_mbar_init();
-  }
-  if (csize > 1) cluster_sync();
-  else __syncthreads();
-  pdl_wait();
-
-  if (warp == NCW) {
-    // ---------------- producer warp: lane 0 issues, in job order
-    if (lane == 0) {
-      int g = 0;
-      bool failed = false;
-      for (int k = 0; k < K; ++k) {
-        const int64_t n = cid + int64_t(k) * ncl;
-        for (int pass = 0; pass < 2; ++pass) {
-          for (int j = 0; j < nch; ++j, ++g) {
-            const int st = g % kEpiStages;
-            const unsigned use = static_cast<unsigned>(g / kEpiStages);
-            // wait until the consumers released this stage's previous use
-            if (!failed && use > 0 && !mbar_wait_bounded(&empty_bar[st], (use - 1) & 1u, p.err))
-              failed = true;
-            const int tv = (vr - j * T) < T ? (vr - j * T) : T;
-            const unsigned bytes = static_cast<unsigned>(tv) * 16u;
-            if (failed) continue;
-            mbar_arrive_expect_tx(&full_bar[st], bytes * static_cast<unsigned>(C));
-            uint4* dst = ring + st * stage_vecs;
-            const float* src = p.x + n * C * S + (v0 + int64_t(j) * T) * 4;
-            for (int c = 0; c < C; ++c)
-              tma_bulk_g2s(dst + int64_t(c) * T, src + int64_t(c) * S, bytes, &full_bar[st]);
-          }
-        }
-      }
-    }
-    __syncwarp();   // the warp reconverges before the aligned cluster barrier
-  } else {
-    // ---------------- consumer warps
-    int g = 0;
-    bool failed = false;
-    auto acquire = [&](int st, unsigned use) {
-      if (!failed && !mbar_wait_bounded(&full_bar[st], use & 1u, p.err)) failed = true;
-    };
-    auto release = [&](int st) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-    };
-    for (int k = 0; k < K; ++k) {
-      const int64_t n = cid + int64_t(k) * ncl;
-      const int b = k & 1;
-      float4* sl = slots + size_t(b) * C * csize;
-      if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
-      // pass 1: statistics
-      Stat acc[kEpiRingCpw];
-#pragma unroll
-      for (int i = 0; i < kEpiRingCpw; ++i) acc[i] = stat_empty();
-      for (int j = 0; j < nch; ++j, ++g) {
-        const int st = g % kEpiStages;
-        acquire(st, static_cast<unsigned>(g / kEpiStages));
-        const int tv = (vr - j * T) < T ? (vr - j * T) : T;
-        const uint4* stg = ring + st * stage_vecs;
-#pragma unroll
-        for (int i = 0; i < kEpiRingCpw; ++i) {
-          const int c = warp + i * NCW;
-          if (c < C) {
-            const uint4* xc = stg + int64_t(c) * T;
-            for (int v = lane; v < tv; v += 32 * 4) {
-              uint4 r[4];
-              int nvalid = 0;
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const bool ok = v + u * 32 < tv;
-                r[u] = ok ? xc[v + u * 32] : make_uint4(0, 0, 0, 0);
-                nvalid += ok ? 4 : 0;
-              }
-              acc[i] = chan_merge(acc[i], tile_stat<float, 4>(r, nvalid));
-            }
-          }
-        }
-        release(st);
-      }
-#pragma unroll
-      for (int i = 0; i < kEpiRingCpw; ++i) {
-        const int c = warp + i * NCW;
-        if (c < C) {   // warp-uniform
-          const Stat a = warp_merge<32>(acc[i]);
-          const float4 v = make_float4(__shfl_sync(kFullMask, a.n, 0), __shfl_sync(kFullMask, a.mean, 0),
-                                       __shfl_sync(kFullMask, a.m2, 0), 0.f);
-          for (unsigned rr = lane; rr < csize; rr += 32)
-            st_async_v4(&sl[size_t(c) * csize + crank], &xbar[b], rr, v);
-        }
-      }
-      // every channel's partials from every rank, merged in rank order
-      if (warp == 0 && !failed &&
-          !mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(k) >> 1) & 1u, p.err))
-        failed = true;
-      named_sync(1, kEpiRingCons);
-      for (int c = warp; c < C; c += NCW) {
-        Stat s2 = stat_empty();
-        if (lane < static_cast<int>(csize)) {
-          const float4 v = sl[size_t(c) * csize + lane];
-          s2 = Stat{v.x, v.y, v.z};
-        }
-        s2 = warp_merge<16>(s2);
-        if (lane == 0) coef[c] = epi_out_coef(s2, __ldg(p.m + c), p.eps, p.lo, p.hi);
-      }
-      named_sync(1, kEpiRingCons);
-      // pass 2: outputs
-      const int tpv = kEpiRingCons / T;            // threads per position vector
-      const int vloc = tid / tpv, h = tid - vloc * tpv;
-      for (int j = 0; j < nch; ++j, ++g) {
-        const int st = g % kEpiStages;
-        acquire(st, static_cast<unsigned>(g / kEpiStages));
-        const int tv = (vr - j * T) < T ? (vr - j * T) : T;
-        const uint4* stg = ring + st * stage_vecs;
-        float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        int arg[4] = {C, C, C, C};
-        if (vloc < tv) {
-          for (int c = h; c < C; c += tpv) {
-            const uint4 u = stg[int64_t(c) * T + vloc];
-            const float4 kk = coef[c];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float z = epi_zc(Elem<float>::get(u, q), kk);
-              if (WANT_ARG) {
-                if (z > best[q]) {
-                  best[q] = z;
-                  arg[q] = c;
-                }
-              } else {
-                best[q] = fmaxf(best[q], z);
-              }
-            }
-          }
-        }
-        release(st);
-        // combine the tpv partial results of each vector (consecutive lanes)
-        for (int off = 1; off < tpv; off <<= 1) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float ob = __shfl_xor_sync(kFullMask, best[q], off);
-            if (WANT_ARG) {
-              const int oa = __shfl_xor_sync(kFullMask, arg[q], off);
-              epi_combine(best[q], arg[q], ob, oa);
-            } else {
-              best[q] = fmaxf(best[q], ob);
-            }
-          }
-        }
-        if (h == 0 && vloc < tv) {
-          const int64_t pos = (v0 + int64_t(j) * T + vloc) * 4;
-          __stcs(reinterpret_cast<float4*>(p.y + n * S + pos), make_float4(best[0], best[1], best[2], best[3]));
-          if (WANT_ARG) {
-            longlong2* ao = reinterpret_cast<longlong2*>(p.argmax + n * S + pos);
-            __stcs(ao, make_longlong2(arg[0], arg[1]));
-            __stcs(ao + 1, make_longlong2(arg[2], arg[3]));
-          }
-        }
-      }
-      named_sync(1, kEpiRingCons);   // coefficients consumed before the next sample
-    }
   }
   pdl_trigger();
   if (csize > 1) cluster_sync();
@@ -872,15 +471,8 @@ __global__ void __launch_bounds__(THREADS) epi_stream_kernel(const EpiParams p) 
 using EpiKernelFn = void (*)(EpiParams);
 
 static EpiKernelFn epi_kernel(const EpiPlan& plan) {
-  if (plan.path == EpiPath::kRing)
-    return plan.threads == kEpiRingThreads
-               ? (plan.want_arg ? &epi_ring_kernel<true> : &epi_ring_kernel<false>)
-               : nullptr;
   if (plan.threads != kEpiThreads) return nullptr;
   switch (plan.path) {
-    case EpiPath::kRange:
-      return plan.want_arg ? &epi_range_kernel<kEpiThreads, true>
-                           : &epi_range_kernel<kEpiThreads, false>;
     case EpiPath::kRangeL2:
       if (plan.keep == kEpiKeepMax) {
         if (plan.onepass)
@@ -894,8 +486,6 @@ static EpiKernelFn epi_kernel(const EpiPlan& plan) {
                              : &epi_range_l2_kernel<kEpiThreads, false, -1, true>;
       return plan.want_arg ? &epi_range_l2_kernel<kEpiThreads, true, -1, false>
                            : &epi_range_l2_kernel<kEpiThreads, false, -1, false>;
-    case EpiPath::kRing:
-      return plan.want_arg ? &epi_ring_kernel<true> : &epi_ring_kernel<false>;
     case EpiPath::kStream: return &epi_stream_kernel<kEpiThreads>;
   }
   return nullptr;

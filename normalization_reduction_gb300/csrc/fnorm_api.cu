@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -72,10 +73,58 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
 
 bool finite_nonneg(float v) { return std::isfinite(v) && v >= 0.f; }
 
-const char* env(const char* name) {
-  const char* v = std::getenv(name);
-  return (v && *v) ? v : nullptr;
+// Tuning and test switches (FNORM_* environment variables) are read once per
+// process, on the first call that needs one, and again only when
+// fnorm_tuning_reload() is called. With none of them set, env() returns at
+// the first branch.
+struct Knob {
+  const char* name;
+  std::string value;
+  bool set;
+};
+Knob g_knobs[] = {
+    {"FNORM_FORCE_PATH", {}, false},      {"FNORM_SPLIT_SHAPE", {}, false},
+    {"FNORM_RESIDENT_THREADS", {}, false}, {"FNORM_FORCE_SCALAR", {}, false},
+    {"FNORM_STREAM_UNROLL", {}, false},   {"FNORM_NO_PACK", {}, false},
+    {"FNORM_EPI_CLUSTER", {}, false},     {"FNORM_EPI_KEEP", {}, false},
+    {"FNORM_EPI_STREAM", {}, false},      {"FNORM_EPI_TWOPASS", {}, false},
+    {"FNORM_BN_SPLIT", {}, false},        {"FNORM_BN_RESIDENT", {}, false},
+    {"FNORM_BN_NO_COLUMNS", {}, false},   {"FNORM_DEBUG_PLAN", {}, false},
+};
+std::mutex g_knob_mutex;
+std::atomic<int> g_knobs_state{0};   // 0: not read, 1: read, none set, 2: read, some set
+
+void load_knobs() {
+  std::lock_guard<std::mutex> lk(g_knob_mutex);
+  bool any = false;
+  for (Knob& k : g_knobs) {
+    const char* v = std::getenv(k.name);
+    k.set = v && *v;
+    k.value = k.set ? v : "";
+    any = any || k.set;
+  }
+  g_knobs_state.store(any ? 2 : 1, std::memory_order_release);
 }
+
+const char* env(const char* name) {
+  int st = g_knobs_state.load(std::memory_order_acquire);
+  if (st == 0) {
+    static std::once_flag once;
+    std::call_once(once, [] {
+      if (g_knobs_state.load(std::memory_order_acquire) == 0) load_knobs();
+    });
+    st = g_knobs_state.load(std::memory_order_acquire);
+  }
+  if (st == 1) return nullptr;
+  for (const Knob& k : g_knobs)
+    if (std::strcmp(k.name, name) == 0) return k.set ? k.value.c_str() : nullptr;
+  return nullptr;
+}
+
+// Test hook (fnorm_debug_force_timeout): one CTA of each launch waits on a
+// barrier that nothing completes, so that its bounded wait expires.
+std::atomic<int> g_force_timeout{0};
+int force_timeout() { return g_force_timeout.load(std::memory_order_relaxed) ? 1 : 0; }
 
 int occupancy_cached(const std::string& key, int (*query)(const void*), const void* arg) {
   const int d = current_device();
@@ -341,22 +390,17 @@ int epi_query(const void* arg) { return epi_max_active_clusters(static_cast<cons
 
 int epi_capacity(const EpiPlan& plan) {
   char key[128];
-  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%d|%d|%zu|%d|%d", static_cast<int>(plan.path),
-                plan.threads, plan.cluster, plan.want_arg ? 1 : 0, plan.ring_t, plan.smem,
+  std::snprintf(key, sizeof key, "epi|%d|%d|%d|%d|%zu|%d|%d", static_cast<int>(plan.path),
+                plan.threads, plan.cluster, plan.want_arg ? 1 : 0, plan.smem,
                 plan.keep == kEpiKeepMax ? 1 : 0, plan.onepass ? 1 : 0);
   EpiQuery q{plan};
   return occupancy_cached(key, epi_query, &q);
 }
 
-constexpr size_t kEpiTargetBytes = 56 * 1024;   // staged bytes per buffer: two CTAs per SM
-
 // Range plans: a cluster of CTAs per sample, each CTA owning a range of
-// positions of all C channels. Default: the L2 form (no staging), 4-CTA
-// clusters. FNORM_EPI_RING=1 selects the TMA ring form (C <= 32);
-// FNORM_EPI_STAGED=1 the staged (double-buffered shared memory) form:
-// preferred cluster sizes in order, the first whose per-buffer staging fits
-// kEpiTargetBytes wins, else the first that fits shared memory.
-// FNORM_EPI_CLUSTER forces a cluster size, FNORM_EPI_STREAM the fallback.
+// positions of all C channels (the L2 form: statistics from HBM, outputs
+// re-read from L2), 4-CTA clusters unless FNORM_EPI_CLUSTER forces a size;
+// FNORM_EPI_STREAM forces the element-wise fallback.
 fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax, int64_t N,
                            int64_t C, int64_t S, EpiPlan* out) {
   const DeviceInfo& di = device_info();
@@ -366,49 +410,9 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   EpiPlan plan{};
   plan.threads = kEpiThreads;
   bool have = false;
-  if (vec && C <= 1024 && env("FNORM_EPI_STAGED")) {
-    const int cands[] = {8, 16, 4, 2, 1};
-    const int64_t nv4 = S / 4;
-    for (int pass = 0; pass < 2 && !have; ++pass) {
-      for (int cl : cands) {
-        if (force_cl && cl != std::atoi(force_cl)) continue;
-        const int64_t per = (nv4 + cl - 1) / cl;
-        const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
-        const size_t smem = epi_range_smem(C, per, cl_eff);
-        const size_t staged = static_cast<size_t>(C) * per * 16;
-        if (smem > static_cast<size_t>(di.max_smem_optin) || staged >= (size_t(1) << 20)) continue;
-        if (pass == 0 && !force_cl && staged > kEpiTargetBytes) continue;
-        EpiPlan cand{EpiPath::kRange, kEpiThreads, cl_eff, per, argmax != nullptr, 0, smem, 0};
-        if (epi_capacity(cand) > 0) {
-          plan = cand;
-          have = true;
-          break;
-        }
-      }
-    }
-  }
-  if (vec && C <= kEpiRingMaxC && !have && env("FNORM_EPI_RING")) {
-    // The TMA ring form (opt-in). Stage = C x T position vectors with
-    // T = 2048 / C rounded down to a power of two in [32, 256] (32 KiB per
-    // stage for C >= 8); 4-CTA clusters unless forced.
-    int T = 256;
-    while (T > 32 && static_cast<int64_t>(T) * C > 2048) T >>= 1;
-    const int cl = force_cl ? std::atoi(force_cl) : 4;
-    const int64_t nv4 = S / 4;
-    const int64_t per = (nv4 + cl - 1) / cl;
-    const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
-    EpiPlan cand{EpiPath::kRing, kEpiRingThreads, cl_eff, per, argmax != nullptr, T,
-                 epi_ring_smem(C, T, cl_eff), 0};
-    if (cl >= 1 && cl <= kMaxCluster && cand.smem <= static_cast<size_t>(di.max_smem_optin) &&
-        epi_capacity(cand) > 0) {
-      plan = cand;
-      have = true;
-    }
-  }
-  if (vec && C <= 1024 && !have) {
-    // Default: the range decomposition without staging -- statistics from
-    // HBM, outputs re-read from L2 (4-CTA clusters keep every sample of the
-    // page's shape resident at once).
+  if (vec && C <= 1024) {
+    // The range decomposition: statistics from HBM, outputs re-read from L2
+    // (4-CTA clusters keep every sample of the page's shape resident at once).
     const int cl = force_cl ? std::atoi(force_cl) : 4;
     const int64_t nv4 = S / 4;
     const int64_t per = (nv4 + cl - 1) / cl;
@@ -418,7 +422,7 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
     if (keep > per) keep = static_cast<int>(per);
     if (const char* k = env("FNORM_EPI_KEEP")) keep = std::atoi(k) < keep ? std::atoi(k) : keep;
     if (keep < 0) keep = 0;
-    EpiPlan cand{EpiPath::kRangeL2, kEpiThreads, cl_eff, per, argmax != nullptr, 0,
+    EpiPlan cand{EpiPath::kRangeL2, kEpiThreads, cl_eff, per, argmax != nullptr,
                  epi_range_l2_smem(C, cl_eff, keep), 0, keep,
                  per <= kEpiOnePassMaxPer && !env("FNORM_EPI_TWOPASS")};
     if (cl >= 1 && cl <= kMaxCluster && epi_capacity(cand) > 0) {
@@ -439,10 +443,11 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
   plan.grid = static_cast<int>(clusters * plan.cluster);
   if (env("FNORM_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "fnorm_instancenorm_epilogue plan: path=%d cluster=%d per=%lld ring_t=%d keep=%d "
-                 "onepass=%d smem=%zu grid=%d capacity=%d\n",
-                 static_cast<int>(plan.path), plan.cluster, static_cast<long long>(plan.per),
-                 plan.ring_t, plan.keep, plan.onepass ? 1 : 0, plan.smem, plan.grid, cap);
+                 "fnorm_instancenorm_epilogue plan: path=%d threads=%d cluster=%d per=%lld "
+                 "keep=%d onepass=%d smem=%zu grid=%d capacity=%d\n",
+                 static_cast<int>(plan.path), plan.threads, plan.cluster,
+                 static_cast<long long>(plan.per), plan.keep, plan.onepass ? 1 : 0, plan.smem,
+                 plan.grid, cap);
   *out = plan;
   return FNORM_OK;
 }
@@ -500,6 +505,10 @@ using namespace fnorm;
 extern "C" {
 
 int fnorm_version(void) { return 100; }
+
+void fnorm_tuning_reload(void) { load_knobs(); }
+
+void fnorm_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
 
 const char* fnorm_status_string(fnorm_status s) {
   switch (s) {
@@ -565,7 +574,7 @@ fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const float* gamm
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
   const InParams p{x,    y,     NC,   S, eps, mean_out, rstd_out, err, gamma, beta, C,
-                   env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0};
+                   force_timeout()};
   return cuda_status(in_launch_dispatch(tin, tout, p, plan, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -614,8 +623,7 @@ fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* 
   p.lo = clamp_lo;
   p.hi = clamp_hi;
   p.per = plan.per;
-  p.debug_timeout = env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0;
-  p.ring_t = plan.ring_t;
+  p.debug_timeout = force_timeout();
   p.keep = plan.keep;
   p.err = err;
   return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
@@ -683,11 +691,37 @@ void bn_fill(BnParams* p, const float* x, float* y, const float* gamma, const fl
   p->vec = aligned(x, 16) && (!y || aligned(y, 16)) && S % 4 == 0 && !env("FNORM_FORCE_SCALAR");
   const char* split = env("FNORM_BN_SPLIT");
   p->split = !(split && split[0] == '0');
-  p->debug_timeout = env("FNORM_DEBUG_FORCE_TIMEOUT") ? 1 : 0;
+  p->debug_timeout = force_timeout();
   p->err = err;
 }
 
 }  // namespace
+
+}  // extern "C"
+
+namespace fnorm {
+
+// Every argument check of fnorm_batchnorm_train except those of the workspace
+// (shared with fnorm_batchnorm_train_noalloc, which validates identically
+// before looking at its scratch size). *total = N*C*S; total == 0 with FNORM_OK
+// is a no-op.
+fnorm_status bn_train_check(const float* x, const float* y, const float* gamma,
+                            const float* beta, float scale, const float* running_mean,
+                            const float* running_var, float momentum, float eps,
+                            const float* save_mean, const float* save_rstd, int64_t N, int64_t C,
+                            int64_t S, int64_t* total) {
+  fnorm_status st = bn_check(x, y, gamma, beta, scale, running_mean, running_var, momentum, eps,
+                             save_mean, save_rstd, N, C, S, total);
+  if (st != FNORM_OK || *total == 0) return st;
+  if (N * S < 2) return FNORM_ERR_INVALID_ARG;   // the unbiased estimate needs two values
+  if (!y) return FNORM_ERR_INVALID_ARG;
+  if (bn_layout(N, C, S).P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
+  return FNORM_OK;
+}
+
+}  // namespace fnorm
+
+extern "C" {
 
 fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma, const float* beta,
                                    float scale, float* running_mean, float* running_var,
@@ -695,14 +729,12 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
                                    int64_t N, int64_t C, int64_t S, void* workspace,
                                    size_t workspace_bytes, fnorm_stream_t stream) {
   int64_t total = 0;
-  fnorm_status st = bn_check(x, y, gamma, beta, scale, running_mean, running_var, momentum, eps,
-                             save_mean, save_rstd, N, C, S, &total);
+  fnorm_status st = bn_train_check(x, y, gamma, beta, scale, running_mean, running_var, momentum,
+                                   eps, save_mean, save_rstd, N, C, S, &total);
   if (st != FNORM_OK || total == 0) return st;
-  if (N * S < 2) return FNORM_ERR_INVALID_ARG;   // the unbiased estimate needs two values
-  if (!y || !workspace) return FNORM_ERR_INVALID_ARG;
+  if (!workspace) return FNORM_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return FNORM_ERR_ALIGNMENT;
   const BnLayout l = bn_layout(N, C, S);
-  if (l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
   if (workspace_bytes < l.ws_bytes) return FNORM_ERR_INVALID_ARG;
   const size_t xb = static_cast<size_t>(total) * 4, cb = static_cast<size_t>(C) * 4,
                wb = l.ws_bytes;

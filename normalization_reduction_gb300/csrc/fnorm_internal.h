@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/fnorm.h"
+
 namespace fnorm {
 
 // Device error word codes (kernels OR them into the word the host passes in).
@@ -83,14 +85,11 @@ struct EpiParams {
   float hi;
   int64_t per;         // position vectors (of 4) per CTA (range path)
   int debug_timeout;   // test hook: wait on an mbarrier nobody completes
-  int ring_t;          // position vectors per ring stage (ring path)
   int keep;            // position vectors per channel kept in shared memory between passes (L2 path)
   unsigned* err;
 };
 
-enum class EpiPath : int { kRange = 0, kStream = 1, kRangeL2 = 2, kRing = 4 };
-constexpr int kEpiRingThreads = 288;   // 8 consumer warps + 1 producer warp
-constexpr int kEpiRingMaxC = 32;       // channels the ring kernel handles
+enum class EpiPath : int { kStream = 1, kRangeL2 = 2 };
 
 struct EpiPlan {
   EpiPath path;
@@ -98,7 +97,6 @@ struct EpiPlan {
   int cluster;
   int64_t per;
   bool want_arg;
-  int ring_t;
   size_t smem;   // dynamic shared memory bytes
   int grid;      // CTAs (multiple of cluster)
   int keep;      // L2 path: position vectors per channel kept on chip
@@ -111,7 +109,6 @@ constexpr int kEpiMaxChannels = 8192;
 
 cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t stream);
 int epi_max_active_clusters(const EpiPlan& plan);
-size_t epi_range_smem(int64_t C, int64_t per, int cluster);
 size_t epi_range_l2_smem(int64_t C, int cluster, int keep);
 // L2 path: the leading position vectors of each channel of a CTA's range that
 // stay in shared memory from the statistics pass to the output pass.
@@ -120,7 +117,6 @@ constexpr int kEpiKeepMax = 160;
 // lane, 160 values) take the shifted one-pass lane sums for the statistics.
 constexpr int64_t kEpiOnePassMaxPer = 1280;
 constexpr int kEpiKeepBudget = 40960;   // bytes (keeps the CTA under 48 KB of dynamic smem)
-size_t epi_ring_smem(int64_t C, int ring_t, int cluster);
 size_t epi_stream_smem(int64_t C, int cluster);
 
 // ---------------------------------------------------------------- BatchNorm
@@ -181,6 +177,14 @@ constexpr int kBnColRows = 32;       // rows per column-statistics partial
 // on chip; returns cudaErrorCooperativeLaunchTooLarge when the grid cannot be
 // co-resident (the caller then uses bn_launch).
 cudaError_t bn_launch_resident(const BnParams& p, cudaStream_t stream);
+
+// fnorm_batchnorm_train's argument checks other than the workspace's (see
+// fnorm_api.cu); *total receives N*C*S.
+fnorm_status bn_train_check(const float* x, const float* y, const float* gamma,
+                            const float* beta, float scale, const float* running_mean,
+                            const float* running_var, float momentum, float eps,
+                            const float* save_mean, const float* save_rstd, int64_t N, int64_t C,
+                            int64_t S, int64_t* total);
 constexpr int64_t kBnEvalFlatBelow = 1024;   // runs shorter than this take the flat eval kernel
 
 // ---------------------------------------------------------------- helpers

@@ -52,3 +52,38 @@ def max_over_ranks(value: float, device=None) -> float:
 def barrier() -> None:
     if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
         tdist.barrier()
+
+
+def free_port() -> int:
+    """A TCP port on 127.0.0.1 that was free a moment ago."""
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_plan(gpus: int, environ, argv, script: str, python: str, port: int | None = None):
+    """How a benchmark asked to run on ``gpus`` GPUs (one process each) starts.
+
+    * not under a launcher (no WORLD_SIZE) and gpus == 1: run here, one rank;
+    * not under a launcher and gpus > 1: re-launch the same command line under
+      ``torch.distributed.run`` with one process per GPU on 127.0.0.1;
+    * under a launcher: run here when WORLD_SIZE equals gpus, else an error.
+
+    Returns a dict with "action" in {"run", "relaunch", "error"} and, for
+    "run", the world size; for "relaunch", the command; for "error", why.
+    """
+    if gpus < 1:
+        return {"action": "error", "why": f"--gpus must be >= 1 (got {gpus})"}
+    ws = environ.get("WORLD_SIZE")
+    if ws is None:
+        if gpus == 1:
+            return {"action": "run", "world_size": 1}
+        cmd = [python, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port or free_port()), script,
+               *argv]
+        return {"action": "relaunch", "cmd": cmd, "world_size": gpus}
+    if int(ws) != gpus:
+        return {"action": "error",
+                "why": f"launched with WORLD_SIZE={ws} processes but --gpus {gpus}"}
+    return {"action": "run", "world_size": gpus}

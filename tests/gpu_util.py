@@ -64,3 +64,44 @@ class Guarded:
         tail = self.buf[self.band + self.n:]
         assert bool((head == CANARY).all()), "write before the output buffer"
         assert bool((tail == CANARY).all()), "write past the output buffer"
+
+
+def check_in_chunks(n_units: int, chunk: int, fetch, check, workers: int | None = None) -> int:
+    """Runs ``check(a, b, fetch(a, b))`` for every chunk [a, b) of ``n_units``.
+
+    ``fetch`` (device -> host copies) runs in the calling thread, ``check``
+    (the oracle and the comparison) in a pool of threads: the oracle's ctypes
+    calls and numpy's array arithmetic release the GIL, so chunks are checked
+    in parallel on the host cores while the next chunk is copied. At most
+    ``2 * workers`` fetched chunks are held at once. Returns the number of
+    chunks checked; any failing check raises here.
+    """
+    import concurrent.futures as cf
+    import os
+
+    workers = workers or max(1, min(8, (os.cpu_count() or 2) - 1))
+    done = 0
+    with cf.ThreadPoolExecutor(max_workers=workers) as pool:
+        pending = []
+        for a in range(0, n_units, chunk):
+            b = min(n_units, a + chunk)
+            host = fetch(a, b)
+            pending.append(pool.submit(check, a, b, host))
+            while len(pending) >= 2 * workers:
+                pending.pop(0).result()
+                done += 1
+        for f in pending:
+            f.result()
+            done += 1
+    return done
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16 or int16) -> float64, exactly."""
+    u = np.ascontiguousarray(bits).view(np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    """A bf16 device tensor's bit patterns on the host (uint16)."""
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)

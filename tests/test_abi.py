@@ -40,6 +40,21 @@ def test_library_exports_every_declared_symbol(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def test_tuning_switches_read_once(lib, monkeypatch):
+    """The FNORM_* switches are read once per process; fnorm_tuning_reload
+    re-reads them, and the forced-timeout hook takes no environment input."""
+    fn.fnorm_tuning_reload()
+    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")   # no longer a switch
+    fn.fnorm_tuning_reload()
+    fn.fnorm_debug_force_timeout(False)
+    monkeypatch.undo()
+    fn.fnorm_tuning_reload()
+    src = open(os.path.join(os.path.dirname(HEADER), "..", "normalization_reduction_gb300", "csrc",
+                            "fnorm_api.cu")).read()
+    assert "FNORM_DEBUG_FORCE_TIMEOUT" not in src
+    assert src.count("std::getenv(") == 1   # only the one-time reader
+
+
 def test_status_strings_and_version(lib):
     for s in fn.Status:
         assert fn.fnorm_status_string(int(s)) == "FNORM_" + s.name
@@ -207,6 +222,8 @@ int call_all(void* x, void* y, float* g, float* m, long long* a, void* ws, fnorm
                                    1e-5f, 0, 0, 2, 3, 64, s);
   st = fnorm_batchnorm_train_noalloc((const float*)x, (float*)y, g, g, 2.f, g, g, 0.1f, 1e-5f,
                                      0, 0, 2, 3, 64, s);
+  fnorm_tuning_reload();
+  fnorm_debug_force_timeout(0);
   printf("%s %d %d\n", fnorm_status_string(st), (int)fnorm_get_last_error(), fnorm_version());
   return (int)st;
 }

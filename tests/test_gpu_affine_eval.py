@@ -79,12 +79,12 @@ AFFINE_FORCED = [
 
 @pytest.mark.parametrize("path,S", AFFINE_FORCED, ids=[p for p, _ in AFFINE_FORCED])
 @pytest.mark.parametrize("scalar", [False, True], ids=["vec", "scalar"])
-def test_affine_forced_paths(orc, monkeypatch, path, S, scalar):
+def test_affine_forced_paths(orc, fnorm_env, path, S, scalar):
     if path.startswith("split") and scalar:
         pytest.skip("the split kernel has vector access only")
-    monkeypatch.setenv("FNORM_FORCE_PATH", path)
+    fnorm_env.setenv("FNORM_FORCE_PATH", path)
     if scalar:
-        monkeypatch.setenv("FNORM_FORCE_SCALAR", "1")
+        fnorm_env.setenv("FNORM_FORCE_SCALAR", "1")
     C = 3
     N = max(2, min(7, 2_000_000 // (S * C)))
     for tin in (torch.float32, torch.bfloat16):
@@ -148,10 +148,10 @@ EVAL_SHAPES = [(2, 3, 1), (4, 5, 7), (3, 4, 100), (2, 3, 1023), (2, 3, 1024), (5
 @pytest.mark.parametrize("scalar", [False, True], ids=["vec", "scalar"])
 @pytest.mark.parametrize("affine", [True, False], ids=["affine", "plain"])
 @pytest.mark.parametrize("staged", ["1", "0"], ids=["staged", "registers"])
-def test_eval_shapes(orc, monkeypatch, shape, scalar, affine, staged):
+def test_eval_shapes(orc, fnorm_env, shape, scalar, affine, staged):
     if scalar:
-        monkeypatch.setenv("FNORM_FORCE_SCALAR", "1")
-    monkeypatch.setenv("FNORM_BN_SPLIT", staged)
+        fnorm_env.setenv("FNORM_FORCE_SCALAR", "1")
+    fnorm_env.setenv("FNORM_BN_SPLIT", staged)
     N, C, S = shape
     x, _, _ = inputs.per_channel_normal((N, C, S), 70_000 + S * C, dev())
     gamma, beta = params(C, 71 + S) if affine else (None, None)

@@ -72,11 +72,11 @@ def test_shapes(orc, shape):
                                    (3, 2, 49152), (9, 64, 15876), (4, 3, 8192), (4, 3, 8196),
                                    (2, 5, 16380)])
 @pytest.mark.parametrize("split", ["1", "0"], ids=["split", "registers"])
-def test_statistics_kernels(orc, monkeypatch, shape, split):
+def test_statistics_kernels(orc, fnorm_env, shape, split):
     """Both vector-mode statistics kernels (registers + TMA staging, registers
     only): runs of many chunks, tiny runs of one vector, units that end in the
     register part, in the staged part and exactly at the chunk size."""
-    monkeypatch.setenv("FNORM_BN_SPLIT", split)
+    fnorm_env.setenv("FNORM_BN_SPLIT", split)
     x, g, b, _, _ = inputs.batchnorm(dev(), shape=shape, seed=11 + shape[-1])
     check(orc, x, g, b, what=f"{shape} split={split}")
 
@@ -86,8 +86,8 @@ def test_no_affine_no_running(orc):
     check(orc, x, None, None, scale=1.0, with_running=False, what="plain")
 
 
-def test_scalar_path(orc, monkeypatch):
-    monkeypatch.setenv("FNORM_FORCE_SCALAR", "1")
+def test_scalar_path(orc, fnorm_env):
+    fnorm_env.setenv("FNORM_FORCE_SCALAR", "1")
     x, g, b, _, _ = inputs.batchnorm(dev(), shape=(4, 6, 1000))
     check(orc, x, g, b, what="scalar")
 
@@ -146,13 +146,13 @@ def test_deterministic():
 
 
 @pytest.mark.parametrize("mode", ["train", "eval"])
-def test_bounded_wait_timeout(orc, monkeypatch, mode):
+def test_bounded_wait_timeout(orc, fnorm_env, mode):
     """The test hook makes one CTA of each staged BatchNorm kernel wait on an
     mbarrier nothing completes: the waits expire, the error word reports
     FNORM_ERR_TIMEOUT (read and cleared) and the results are still correct."""
     assert fn.fnorm_get_last_error() == fn.Status.OK
     x, g, b, _, _ = inputs.batchnorm(dev(), shape=(6, 5, 3000))
-    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    fnorm_env.force_timeout(True)
     if mode == "train":
         y, _, _ = run_bn(x, g, b, None, None)
         ref, _, _, _, _ = orc.batchnorm_train(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(),
@@ -167,26 +167,26 @@ def test_bounded_wait_timeout(orc, monkeypatch, mode):
                                  rm.cpu().numpy(), rv.cpu().numpy(), EPS)
     assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
     assert fn.fnorm_get_last_error() == fn.Status.OK
-    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    fnorm_env.force_timeout(False)
     assert_close(y.cpu().numpy(), ref, torch.float32, f"{mode} after timeout")
 
 
 @pytest.mark.parametrize("shape", [(8, 64, 126, 126), (2, 1, 100000), (300, 3, 4), (5, 7, 36),
                                    (4, 3, 8196), (1, 2, 5), (3, 40, 16384), (64, 3, 100)])
-def test_resident_kernel(orc, monkeypatch, shape):
+def test_resident_kernel(orc, fnorm_env, shape):
     """The single cooperative launch (statistics, grid barrier, apply with
     each CTA's last unit kept in shared memory) against the oracle: more
     units than CTAs, fewer units than CTAs, units of several chunks, tiny
     units, element-wise fall-back shapes (S % 4 != 0 take the two launches)."""
-    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+    fnorm_env.setenv("FNORM_BN_RESIDENT", "1")
     x, g, b, _, _ = inputs.batchnorm(dev(), shape=shape, seed=31 + shape[1])
     check(orc, x, g, b, what=f"resident {shape}")
 
 
-def test_resident_dirty_workspace_and_repeat(orc, monkeypatch):
+def test_resident_dirty_workspace_and_repeat(orc, fnorm_env):
     """The barrier counter lives in the caller's workspace, which needs no
     clearing: garbage between calls, and back-to-back calls on one stream."""
-    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+    fnorm_env.setenv("FNORM_BN_RESIDENT", "1")
     x, g, b, _, _ = inputs.batchnorm(dev(), shape=(16, 8, 3000))
     nbytes = fn.fnorm_batchnorm_workspace_size(16, 8, 3000)
     ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=dev())
@@ -197,20 +197,20 @@ def test_resident_dirty_workspace_and_repeat(orc, monkeypatch):
         assert_close(y.cpu().numpy(), ref, torch.float32, "resident, dirty workspace")
         ws.fill_(0x5A)
     y1, _, _ = run_bn(x, g, b, None, None, workspace=ws)
-    monkeypatch.delenv("FNORM_BN_RESIDENT")
+    fnorm_env.delenv("FNORM_BN_RESIDENT")
     y2, _, _ = run_bn(x, g, b, None, None, workspace=ws)
     assert torch.equal(y1, y2)   # same partials, same merge order: same bits as two launches
 
 
-def test_resident_timeout_hook(orc, monkeypatch):
-    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+def test_resident_timeout_hook(orc, fnorm_env):
+    fnorm_env.setenv("FNORM_BN_RESIDENT", "1")
     assert fn.fnorm_get_last_error() == fn.Status.OK
     x, g, b, _, _ = inputs.batchnorm(dev(), shape=(6, 5, 3000))
-    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    fnorm_env.force_timeout(True)
     y, _, _ = run_bn(x, g, b, None, None)
     assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
     assert fn.fnorm_get_last_error() == fn.Status.OK
-    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    fnorm_env.force_timeout(False)
     ref, _, _, _, _ = orc.batchnorm_train(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(), 2.0,
                                           None, None, MOM, EPS)
     assert_close(y.cpu().numpy(), ref, torch.float32, "resident after timeout")
@@ -219,12 +219,12 @@ def test_resident_timeout_hook(orc, monkeypatch):
 @pytest.mark.parametrize("shape", [(4096, 64, 1), (1000, 3, 7), (33, 17, 3), (31, 5, 16),
                                    (100000, 2, 1), (1, 2, 16), (2, 1, 1), (65, 300, 2)])
 @pytest.mark.parametrize("columns", ["1", "0"], ids=["columns", "units"])
-def test_short_runs(orc, monkeypatch, shape, columns):
+def test_short_runs(orc, fnorm_env, shape, columns):
     """Runs of at most 16 values (BatchNorm over [N, C] and small maps): the
     column form (column statistics over row blocks, channel merge, apply) and
     the per-unit form agree with the oracle, running statistics included."""
     if columns == "0":
-        monkeypatch.setenv("FNORM_BN_NO_COLUMNS", "1")
+        fnorm_env.setenv("FNORM_BN_NO_COLUMNS", "1")
     x, g, b, _, _ = inputs.batchnorm(dev(), shape=shape, seed=41 + shape[0])
     check(orc, x, g, b, what=f"short runs {shape} columns={columns}")
 

@@ -50,38 +50,24 @@ def test_page_shape_subset(orc):
     check(orc, x, m, what="page shape")
 
 
-@pytest.mark.parametrize("staged", [False, True], ids=["l2", "staged"])
 @pytest.mark.parametrize("cl", [1, 2, 4, 8, 16])
-def test_cluster_sizes(orc, monkeypatch, cl, staged):
-    """Both range kernels (L2 re-read and double-buffered staging) at every
-    cluster size; staged plans that do not fit fall back to the stream kernel."""
-    monkeypatch.setenv("FNORM_EPI_CLUSTER", str(cl))
-    if staged:
-        monkeypatch.setenv("FNORM_EPI_STAGED", "1")
+def test_cluster_sizes(orc, fnorm_env, cl):
+    """The range kernel at every cluster size."""
+    fnorm_env.setenv("FNORM_EPI_CLUSTER", str(cl))
     x, m = inputs.epilogue(dev(), shape=(5, 16, 14, 30, 30))
     check(orc, x, m, what=f"cluster {cl}")
-
-
-@pytest.mark.parametrize("variant", ["FNORM_EPI_STAGED", "FNORM_EPI_RING"])
-@pytest.mark.parametrize("shape", [(4, 16, 14, 30, 30), (3, 5, 1000), (2, 1, 4096), (3, 32, 1000),
-                                   (2, 9, 4)])
-def test_variant_shapes(orc, monkeypatch, shape, variant):
-    """The staged and TMA-ring range kernels on several shapes."""
-    monkeypatch.setenv(variant, "1")
-    x, m = inputs.epilogue(dev(), shape=shape, seed=4321 + shape[1])
-    check(orc, x, m, what=f"{variant} {shape}")
 
 
 @pytest.mark.parametrize("keep", ["0", "1", "37", "160"])
 @pytest.mark.parametrize("shape", [(4, 16, 14, 30, 30), (3, 5, 1000), (2, 1, 4096), (3, 40, 1000),
                                    (2, 9, 4), (2, 3, 2052)])
 @pytest.mark.parametrize("cl", ["2", "4"])
-def test_l2_keep_sizes(orc, monkeypatch, shape, keep, cl):
+def test_l2_keep_sizes(orc, fnorm_env, shape, keep, cl):
     """The L2-form kernel with 0 .. 160 position vectors per channel kept in
     shared memory between its passes (ranges shorter and longer than the kept
     part, kept parts that end inside a tile)."""
-    monkeypatch.setenv("FNORM_EPI_KEEP", keep)
-    monkeypatch.setenv("FNORM_EPI_CLUSTER", cl)
+    fnorm_env.setenv("FNORM_EPI_KEEP", keep)
+    fnorm_env.setenv("FNORM_EPI_CLUSTER", cl)
     x, m = inputs.epilogue(dev(), shape=shape, seed=777 + shape[1])
     check(orc, x, m, what=f"keep {keep} {shape} cl {cl}")
 
@@ -92,24 +78,6 @@ def test_more_samples_than_clusters(orc, shape):
     several samples in turn (alternating exchange slots and barrier phases)."""
     x, m = inputs.epilogue(dev(), shape=shape, seed=600 + shape[0])
     check(orc, x, m, what=f"many samples {shape}")
-
-
-@pytest.mark.parametrize("cl", [1, 2, 4, 8])
-def test_ring_cluster_sizes(orc, monkeypatch, cl):
-    monkeypatch.setenv("FNORM_EPI_RING", "1")
-    monkeypatch.setenv("FNORM_EPI_CLUSTER", str(cl))
-    x, m = inputs.epilogue(dev(), shape=(5, 16, 14, 30, 30))
-    check(orc, x, m, what=f"ring cluster {cl}")
-
-
-def test_ring_timeout_hook(orc, monkeypatch):
-    monkeypatch.setenv("FNORM_EPI_RING", "1")
-    test_bounded_wait_timeout(orc, monkeypatch)
-
-
-def test_staged_timeout_hook(orc, monkeypatch):
-    monkeypatch.setenv("FNORM_EPI_STAGED", "1")
-    test_bounded_wait_timeout(orc, monkeypatch)
 
 
 @pytest.mark.parametrize("shape", [(3, 1, 64), (2, 3, 100), (4, 5, 12), (2, 7, 1000),
@@ -127,8 +95,8 @@ def test_shapes_stream(orc, shape):
     check(orc, x, m, what=str(shape))
 
 
-def test_forced_stream(orc, monkeypatch):
-    monkeypatch.setenv("FNORM_EPI_STREAM", "1")
+def test_forced_stream(orc, fnorm_env):
+    fnorm_env.setenv("FNORM_EPI_STREAM", "1")
     x, m = inputs.epilogue(dev(), shape=(4, 16, 14, 30, 30))
     check(orc, x, m, what="forced stream")
 
@@ -183,17 +151,17 @@ def test_no_argmax_output(orc):
     assert_close(y.cpu().numpy(), ref, torch.float32, "no argmax")
 
 
-def test_bounded_wait_timeout(orc, monkeypatch):
+def test_bounded_wait_timeout(orc, fnorm_env):
     """The test hook makes one CTA wait on an mbarrier nothing completes: the
     wait expires after its limit, the error word reports FNORM_ERR_TIMEOUT,
     the context stays usable and the results are still correct."""
     assert fn.fnorm_get_last_error() == fn.Status.OK
-    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    fnorm_env.force_timeout(True)
     x, m = inputs.epilogue(dev(), shape=(2, 16, 14, 30, 30))
     y, arg = run_epi(x, m)
     assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
     assert fn.fnorm_get_last_error() == fn.Status.OK   # read-and-clear
-    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    fnorm_env.force_timeout(False)
     ref, _, _ = orc.epilogue(x.cpu().numpy().reshape(2, 16, -1), m.cpu().numpy(), EPS)
     assert_close(y.cpu().numpy(), ref, torch.float32, "after timeout")
     check(orc, x, m, what="after timeout")
@@ -234,7 +202,7 @@ def test_saturated_channels_no_index(orc):
 @pytest.mark.parametrize("S", [4096, 20480, 40000])
 @pytest.mark.parametrize("want_arg", [True, False], ids=["index", "no_index"])
 @pytest.mark.parametrize("form", ["default", "twopass"])
-def test_outliers_at_lane_shifts(orc, monkeypatch, S, want_arg, form):
+def test_outliers_at_lane_shifts(orc, fnorm_env, S, want_arg, form):
     """For CTA ranges of at most 1280 vectors (S = 20480 with the default
     4-CTA split: 40 vectors per lane) the statistics are per-lane sums shifted
     by the lane's first value; longer ranges, and every range with
@@ -243,7 +211,7 @@ def test_outliers_at_lane_shifts(orc, monkeypatch, S, want_arg, form):
     lane of every CTA range, on data with a large offset; the outputs must
     still match the oracle."""
     if form == "twopass":
-        monkeypatch.setenv("FNORM_EPI_TWOPASS", "1")
+        fnorm_env.setenv("FNORM_EPI_TWOPASS", "1")
     N, C = 2, 3
     g = torch.Generator().manual_seed(4242 + S)
     x = (torch.randn(N, C, S, generator=g) * 0.5 + 50.0)

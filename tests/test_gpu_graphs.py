@@ -91,9 +91,9 @@ def test_graph_batchnorm_train_and_eval():
     _capture_and_compare(run, [y, ye, sm, sr, rm, rv])
 
 
-def test_graph_batchnorm_resident(monkeypatch):
+def test_graph_batchnorm_resident(fnorm_env):
     """The single cooperative BatchNorm launch (with its counter reset) in a graph."""
-    monkeypatch.setenv("FNORM_BN_RESIDENT", "1")
+    fnorm_env.setenv("FNORM_BN_RESIDENT", "1")
     test_graph_batchnorm_train_and_eval()
 
 

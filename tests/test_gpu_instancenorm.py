@@ -101,7 +101,7 @@ FORCED = [
 
 @pytest.mark.parametrize("path,sizes", FORCED, ids=[p for p, _ in FORCED])
 @pytest.mark.parametrize("scalar", [False, True], ids=["vec", "scalar"])
-def test_forced_paths(orc, monkeypatch, path, sizes, scalar):
+def test_forced_paths(orc, fnorm_env, path, sizes, scalar):
     """Every kernel shape, including empty CTAs in a cluster and 16-CTA clusters."""
     parts = path.split(":")
     if parts[0] == "split" and scalar:
@@ -112,9 +112,9 @@ def test_forced_paths(orc, monkeypatch, path, sizes, scalar):
         forced = path + ":1"
     else:
         forced = path
-    monkeypatch.setenv("FNORM_FORCE_PATH", forced)
+    fnorm_env.setenv("FNORM_FORCE_PATH", forced)
     if scalar:
-        monkeypatch.setenv("FNORM_FORCE_SCALAR", "1")
+        fnorm_env.setenv("FNORM_FORCE_SCALAR", "1")
     for S in sizes:
         for tin in (torch.float32, torch.bfloat16):
             W = 4 if tin == torch.float32 else 8
@@ -220,18 +220,18 @@ def test_mixed_scale_slices(orc):
     assert_close(to_f64(y), ref, torch.float32, "mixed scales")
 
 
-def test_bounded_wait_timeout(orc, monkeypatch):
+def test_bounded_wait_timeout(orc, fnorm_env):
     """The test hook makes one CTA of the split kernel wait, after its last
     cluster barrier, on an mbarrier nothing completes: the wait expires after
     its limit, the error word reports FNORM_ERR_TIMEOUT (read and cleared), the
     context stays usable and the results are correct."""
     assert fn.fnorm_get_last_error() == fn.Status.OK
-    monkeypatch.setenv("FNORM_DEBUG_FORCE_TIMEOUT", "1")
+    fnorm_env.force_timeout(True)
     x = make_x(48, 200000, torch.float32, 515)   # split kernel, 2-CTA clusters
     y, _, _ = run_in(x)
     assert fn.fnorm_get_last_error() == fn.Status.ERR_TIMEOUT
     assert fn.fnorm_get_last_error() == fn.Status.OK
-    monkeypatch.delenv("FNORM_DEBUG_FORCE_TIMEOUT")
+    fnorm_env.force_timeout(False)
     ref, _, _ = oracle_in(orc, x)
     assert_close(to_f64(y), ref, torch.float32, "after timeout")
     y2, _, _ = run_in(x)
@@ -260,7 +260,7 @@ PACKED_CASES = [(3, 1 << 20, None), (2, 1047776, None), (3, 300000, "split:256:8
                          ids=[f"{n}x{s}-{p or 'default'}" for n, s, p in PACKED_CASES])
 @pytest.mark.parametrize("tout", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("dist", ["normal", "shifted"])
-def test_bf16_packed_matches_scalar(orc, monkeypatch, NC, S, path, tout, dist):
+def test_bf16_packed_matches_scalar(orc, fnorm_env, NC, S, path, tout, dist):
     """bf16 slices spread over clusters of more than 8 CTAs take one pass of
     shifted sums and packed pair arithmetic (two fp32 lanes per instruction);
     FNORM_NO_PACK=1 gives the exact two-pass scalar loops. Both must match the
@@ -268,10 +268,10 @@ def test_bf16_packed_matches_scalar(orc, monkeypatch, NC, S, path, tout, dist):
     last case (8-CTA clusters) runs the scalar loops both times and must be
     bit-identical."""
     if path:
-        monkeypatch.setenv("FNORM_FORCE_PATH", path)
+        fnorm_env.setenv("FNORM_FORCE_PATH", path)
     x = make_x(NC, S, torch.bfloat16, 5150 + S % 997, dist)
     y1, m1, r1 = run_in(x, out_dtype=tout, stats=True)
-    monkeypatch.setenv("FNORM_NO_PACK", "1")
+    fnorm_env.setenv("FNORM_NO_PACK", "1")
     y2, m2, r2 = run_in(x, out_dtype=tout, stats=True)
     ref, rmean, rvar = oracle_in(orc, x)
     for y, m, r, what in ((y1, m1, r1, "packed"), (y2, m2, r2, "scalar")):

@@ -81,3 +81,26 @@ def test_empty_shard_stats_are_identity():
     fn.fnorm_batchnorm_local_stats(x, out, 0, 5, 7, None, 0)
     torch.cuda.synchronize()
     assert bool((out == 0).all())
+
+
+def test_single_process_on_a_side_stream(orc):
+    """The library calls on a stream other than torch's current one: the
+    inputs are written on the current stream just before the call, and the
+    result equals the oracle once the side stream is synchronised."""
+    x, g, b, rm, rv = inputs.batchnorm(dev(), shape=(6, 8, 20, 20), seed=9)
+    x2 = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    rm0, rv0 = rm.cpu().numpy(), rv.cpu().numpy()
+    for _ in range(3):
+        x2.copy_(x)                     # on the current stream
+        rm.copy_(torch.from_numpy(rm0).to(dev()))
+        rv.copy_(torch.from_numpy(rv0).to(dev()))
+        y = syncbn.sync_batch_norm_train(x2, g, b, rm, rv, MOM, EPS, SCALE, stream=side)
+        x2.fill_(1e30)                  # the next step's writes, ordered after the call
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        ref, rmo, rvo, _, _ = orc.batchnorm_train(x.cpu().numpy().reshape(6, 8, 400),
+                                                  g.cpu().numpy(), b.cpu().numpy(), SCALE,
+                                                  rm0, rv0, MOM, EPS)
+        assert_close(y.cpu().numpy().reshape(6, 8, 400), ref, torch.float32, "side stream")
+        assert np.max(np.abs(rm.cpu().numpy() - rmo)) <= 1e-6

@@ -3,10 +3,13 @@ cannot allocate device memory (fixed memory budgets, plugins whose host owns
 the allocator, loops where a synchronising cudaMalloc is not allowed). It
 uses the library's own static device scratch instead of a caller workspace.
 
-Its results must match fnorm_batchnorm_train's within the parity tolerance,
-on two calls in a row (the second call finds the scratch holding the first
-call's partials). This file is collected last so that a run stopping at the
-first failure has already run every other test.
+Both entry points run the same kernels on the same partial-statistics layout,
+so the results must be bit-identical, call after call: a small shape, then a
+large one, then a shape of runs of at most 16 values (the column form, which
+keeps its coefficients at another offset of the scratch), then the small one
+again -- so that later calls read scratch regions that earlier calls left
+holding other partials. This file is collected last so that a run stopping at
+the first failure has already run every other test.
 """
 import numpy as np
 import pytest
@@ -17,7 +20,6 @@ from normalization_reduction_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-4   # max-abs, as in the other fp32 parity tests
 SCRATCH_BYTES = 2 << 20
 
 
@@ -41,17 +43,37 @@ def _no_alloc(x, g, b, rm, rv):
     return y, sm, sr
 
 
-@pytest.mark.parametrize("shapes", [[(8, 64, 126, 126), (4, 6, 1000)]])
+@pytest.mark.parametrize("shapes", [[(4, 6, 1000), (8, 64, 126, 126), (64, 8, 4),
+                                     (4, 6, 1000)]])
 def test_no_alloc_matches_workspace_entry_point(shapes):
     dev = torch.device("cuda", torch.cuda.current_device())
-    for i, shape in enumerate(shapes):          # two calls in a row
+    for i, shape in enumerate(shapes):          # calls in a row on the shared scratch
         x, g, b, rm, rv = inputs.batchnorm(dev, shape=shape, seed=500 + i)
         rm_a, rv_a, rm_b, rv_b = rm.clone(), rv.clone(), rm.clone(), rv.clone()
         y_a, sm_a, sr_a = _with_workspace(x, g, b, rm_a, rv_a)
         y_b, sm_b, sr_b = _no_alloc(x, g, b, rm_b, rv_b)
         torch.cuda.synchronize()
         for a, b_ in ((y_a, y_b), (sm_a, sm_b), (sr_a, sr_b), (rm_a, rm_b), (rv_a, rv_b)):
-            assert float((a - b_).abs().max()) <= TOL
+            assert torch.equal(a, b_), shape
+
+
+def test_no_alloc_validates_like_the_workspace_entry_point():
+    """Argument errors are those of fnorm_batchnorm_train even for shapes too
+    large for the scratch (the size check comes after the validation)."""
+    N, C, S = 4096, 64, 4
+    assert fn.fnorm_batchnorm_workspace_size(N, C, S) > SCRATCH_BYTES
+    fake = 1 << 40   # never dereferenced: every call below fails validation first
+    cases = [dict(eps=-1.0), dict(y=None), dict(x=fake + 2)]
+    for kw in cases:
+        a = dict(x=fake, y=fake + (1 << 32), eps=1e-5)
+        a.update(kw)
+        with pytest.raises(fn.FnormError) as e1:
+            fn.fnorm_batchnorm_train_noalloc(a["x"], a["y"], None, None, 1.0, None, None, 0.1,
+                                             a["eps"], None, None, N, C, S)
+        with pytest.raises(fn.FnormError) as e2:
+            fn.fnorm_batchnorm_train(a["x"], a["y"], None, None, 1.0, None, None, 0.1, a["eps"],
+                                     None, None, N, C, S, fake + (1 << 36), 1 << 30)
+        assert e1.value.status == e2.value.status != fn.Status.ERR_UNSUPPORTED, kw
 
 
 def test_no_alloc_rejects_shapes_beyond_the_scratch():
