@@ -3,6 +3,7 @@ x once, write y once) and the fraction of the measured HBM peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--shape N,C,H,W] [--no-extra] [--dry-run]
+                    [--phases]
 
 ``--gpus N`` runs one process per GPU: launched without torchrun, the script
 re-launches itself under ``torch.distributed.run`` with N processes; under a
@@ -57,6 +58,9 @@ NCU_TRAFFIC = {
     # both launches of a training BatchNorm step (caches flushed between them
     # by ncu, so without the apply pass's L2 reuse)
     "batchnorm2d_train_fp32_128x64x126x126": 1506137856,
+    # the L2-form epilogue kernel at full size: 110.260224 MB read + 3.575296 MB
+    # written (the rest of y still dirty in L2 at kernel end)
+    "epilogue_fp32_128x16x14x30x30": 113835520,
 }
 
 
@@ -514,8 +518,44 @@ def cpu_baseline(x_dev: torch.Tensor, S: int, budget_s: float = 10.0, batch: int
             "sample": f"{done} of {NC} slices ({done * S} elements), float64 single-threaded"}
 
 
+PHASE_NAMES = ["statistics", "exchange", "coefficients", "kept_output", "l2_output"]
+
+
+def epilogue_phases():
+    """Per-phase times of the L2-form epilogue kernel's last launch, from the
+    instrumented library (libfnorm_phases.so): median duration of each phase
+    over the CTAs, and each phase's end relative to the earliest CTA start."""
+    import ctypes
+    import numpy as np
+    lib = fn.lib()
+    n_ctas, n_ph = 2048, len(PHASE_NAMES) + 1
+    buf = (ctypes.c_ulonglong * (n_ctas * n_ph))()
+    lib.fnorm_phase_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.fnorm_phase_trace_read.restype = ctypes.c_int
+    if lib.fnorm_phase_trace_read(ctypes.addressof(buf), n_ctas * n_ph) != 0:
+        return {"error": "trace read failed"}
+    t = np.frombuffer(buf, dtype=np.uint64).astype(np.int64).reshape(n_ctas, n_ph)
+    t = t[(t > 0).all(axis=1)]
+    if not len(t):
+        return {"error": "no stamps (not the L2-form kernel?)"}
+    d = np.diff(t, axis=1)
+    t0 = t[:, 0].min()
+    out = {"ctas": int(len(t)), "unit": "us"}
+    for j, name in enumerate(PHASE_NAMES):
+        end = t[:, j + 1] - t0
+        out[name] = {"median": round(float(np.median(d[:, j])) / 1e3, 3),
+                     "end_min": round(float(end.min()) / 1e3, 3),
+                     "end_median": round(float(np.median(end)) / 1e3, 3),
+                     "end_max": round(float(end.max()) / 1e3, 3)}
+    return out
+
+
 def run_ours(args):
     ws, rank, local = dist_info()
+    if args.phases:
+        # the instrumented library: per-phase stamps (timing is perturbed a little)
+        from normalization_reduction_gb300 import build as nbuild
+        fn.LIBRARY = nbuild.build(phases=True)
     if ws > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
@@ -549,6 +589,10 @@ def run_ours(args):
     }
     if args.warmup_requested != args.warmup:
         res["warmup_requested"] = args.warmup_requested
+    if args.phases:
+        res["phases"] = epilogue_phases() if isinstance(wl, Epilogue) else {
+            "error": "phase stamps exist for the epilogue workload only"}
+        res["phases"]["library"] = "libfnorm_phases.so (instrumented)"
     res["dtype"] = wl.dtype
     if rank == 0 and not args.no_extra and isinstance(wl, InstanceNormLarge):
         res["e2e"] = e2e_instancenorm(wl, max(2, min(args.steps, 5)))
@@ -636,6 +680,9 @@ def main():
                          "floor_read:BYTES | floor_copy:BYTES (torch reference floors)")
     ap.add_argument("--shape", default=None,
                     help="N,C,H,W for in_large (e.g. a smaller case for ncu)")
+    ap.add_argument("--phases", action="store_true",
+                    help="epilogue workload: time it with the instrumented library and add "
+                         "the per-phase breakdown of the last launch")
     ap.add_argument("--dry-run", action="store_true",
                     help="print how the run would start (one line of JSON) and exit")
     args = ap.parse_args()

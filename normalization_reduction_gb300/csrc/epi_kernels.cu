@@ -35,6 +35,24 @@
 
 namespace fnorm {
 
+// Instrumented builds only (build.py --phases defines FNORM_PHASE_TRACE; the
+// product library has none of this): thread 0 of each of the first
+// kEpiPhaseCtas CTAs of the L2-form kernel records the %globaltimer value at
+// each phase boundary of its first sample -- start, statistics done, partials
+// exchanged, coefficients formed, kept part written, sample done -- into
+// g_epi_phase[cta][phase], read by fnorm_phase_trace_read (each launch
+// overwrites the previous one's stamps).
+constexpr int kEpiPhases = 6;
+constexpr int kEpiPhaseCtas = 2048;
+#ifdef FNORM_PHASE_TRACE
+__device__ unsigned long long g_epi_phase[kEpiPhaseCtas * kEpiPhases];
+#define FNORM_EPI_STAMP(k)                                                      \
+  if (tid == 0 && it == 0 && blockIdx.x < kEpiPhaseCtas)                      \
+    g_epi_phase[blockIdx.x * kEpiPhases + (k)] = globaltimer_ns();
+#else
+#define FNORM_EPI_STAMP(k)
+#endif
+
 size_t epi_range_l2_smem(int64_t C, int cluster, int keep) {
   return static_cast<size_t>(C) * 16 + 2 * static_cast<size_t>(C) * cluster * 16 +
          static_cast<size_t>(C) * keep * 16 + ((static_cast<size_t>(C) * 4 + 15) & ~size_t(15));
@@ -244,6 +262,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
     const int b = it & 1;
     float4* sl = slots + size_t(b) * C * csize;
     if (tid == 0) mbar_arrive_expect_tx(&xbar[b], static_cast<unsigned>(C) * csize * 16u);
+    FNORM_EPI_STAMP(0)
     const uint4* xn = reinterpret_cast<const uint4*>(p.x + n * C * S) + v0;
     for (int c = warp; c < C; c += NWARP) {
       const uint4* xc = xn + int64_t(c) * nv4 + lane;
@@ -313,10 +332,12 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
     }
     // Warps park at the CTA barrier while one warp waits for the partials.
     __syncthreads();
+    FNORM_EPI_STAMP(1)
     bool ok = true;
     if (warp == 0 && !xfailed)
       ok = mbar_wait_bounded(&xbar[b], (static_cast<unsigned>(it) >> 1) & 1u, p.err);
     if (__syncthreads_or(!ok)) xfailed = true;
+    FNORM_EPI_STAMP(2)
     // Channel coefficients: segments of W lanes (W = csize rounded up to a
     // power of two) each merge one channel's csize partials in a fixed tree
     // (the same bits in every CTA), so a warp does 32/W channels at once.
@@ -339,6 +360,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       }
     }
     __syncthreads();
+    FNORM_EPI_STAMP(3)
     const int vk = vr < KS ? vr : KS;
     for (int v = tid; v < vk; v += THREADS) {   // positions kept on chip
       float best[4];
@@ -362,6 +384,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
         __stcs(ao + 1, make_longlong2(arg[2], arg[3]));
       }
     }
+    FNORM_EPI_STAMP(4)
     for (int v = vk + tid; v < vr; v += THREADS) {
       const uint4* xv = xn + v;
       float best[4];
@@ -395,6 +418,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       }
     }
     __syncthreads();   // coefficients consumed before the next sample rewrites them
+    FNORM_EPI_STAMP(5)
   }
   pdl_trigger();
   if (csize > 1) cluster_sync();
@@ -547,3 +571,14 @@ cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t str
 }
 
 }  // namespace fnorm
+
+#ifdef FNORM_PHASE_TRACE
+// Instrumented builds only: copies the first n phase stamps (see
+// g_epi_phase) to host memory; returns the CUDA error code.
+extern "C" __attribute__((visibility("default"))) int fnorm_phase_trace_read(
+    unsigned long long* out, int n) {
+  if (n > fnorm::kEpiPhaseCtas * fnorm::kEpiPhases) n = fnorm::kEpiPhaseCtas * fnorm::kEpiPhases;
+  return static_cast<int>(
+      cudaMemcpyFromSymbol(out, fnorm::g_epi_phase, sizeof(unsigned long long) * n));
+}
+#endif
