@@ -115,7 +115,7 @@ class Epilogue(Workload):
     kernel = "epi_range_l2_kernel"
     graph = True   # ~30 us per step: timed as a CUDA graph of `steps` launches
 
-    def __init__(self, dev, copies=None):
+    def __init__(self, dev, copies=None, want_arg=False):
         x, m = inputs.epilogue(dev)
         self.N, self.C = x.shape[0], x.shape[1]
         self.S = x[0, 0].numel()
@@ -123,11 +123,17 @@ class Epilogue(Workload):
         copies = copies or max(1, -(-4 * L2_BYTES // nbytes))   # rotate >= 4x L2
         self.xs = [x] + [x.clone() for _ in range(copies - 1)]
         self.ys = [torch.empty((self.N, self.S), device=dev) for _ in range(copies)]
+        # with the argmax output (int64 channel index per position)
+        self.args = ([torch.empty((self.N, self.S), dtype=torch.int64, device=dev)
+                      for _ in range(copies)] if want_arg else None)
+        if want_arg:
+            self.name = self.name + "_argmax"
         self.m = m
         self.i = 0
 
     def bytes_per_step(self):
-        return self.N * self.C * self.S * 4 + self.N * self.S * 4 + self.C * 4
+        b = self.N * self.C * self.S * 4 + self.N * self.S * 4 + self.C * 4
+        return b + (self.N * self.S * 8 if self.args is not None else 0)
 
     def l2_note(self):
         return f"{len(self.xs)} rotating input/output copies (>= 4x L2)"
@@ -135,8 +141,9 @@ class Epilogue(Workload):
     def step(self, stream):
         k = self.i % len(self.xs)
         self.i += 1
-        fn.fnorm_instancenorm_epilogue(self.xs[k], self.m, self.ys[k], None, self.N, self.C,
-                                       self.S, 1e-5, -1.0, 1.0, stream)
+        fn.fnorm_instancenorm_epilogue(self.xs[k], self.m, self.ys[k],
+                                       self.args[k] if self.args is not None else None, self.N,
+                                       self.C, self.S, 1e-5, -1.0, 1.0, stream)
 
 
 class BatchNorm(Workload):
@@ -330,6 +337,8 @@ def make_workload(args, dev) -> Workload:
         return InstanceNormLarge(dev, shape or inputs.SHAPE_LARGE)
     if args.workload == "epilogue":
         return Epilogue(dev)
+    if args.workload == "epilogue_argmax":
+        return Epilogue(dev, want_arg=True)
     if args.workload == "batchnorm":
         return BatchNorm(dev)
     if args.workload == "in_affine":
@@ -611,6 +620,7 @@ def other_configs(dev, ws, peak):
     """The other workloads, same timing rules (reported alongside)."""
     out = {}
     cases = [("epilogue", lambda: Epilogue(dev), 200, 20),
+             ("epilogue_argmax", lambda: Epilogue(dev, want_arg=True), 200, 20),
              ("batchnorm", lambda: BatchNorm(dev), 20, 5),
              ("batchnorm_eval", lambda: BatchNormEval(dev), 20, 5),
              ("instancenorm_affine", lambda: InstanceNormAffine(dev), 20, 5)]
@@ -675,7 +685,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip e2e, cpu baseline and the other workloads")
     ap.add_argument("--workload", default="in_large",
-                    help="in_large | in_affine | epilogue | batchnorm | bn_eval | sweep:S[:TOTAL] "
+                    help="in_large | in_affine | epilogue | epilogue_argmax | batchnorm | bn_eval | "
+                         "sweep:S[:TOTAL] "
                          "(S a power of 4, 256..4^10; TOTAL elements, default 2^30) | "
                          "floor_read:BYTES | floor_copy:BYTES (torch reference floors)")
     ap.add_argument("--shape", default=None,
