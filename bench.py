@@ -168,6 +168,21 @@ class BatchNorm(Workload):
                                  stream)
 
 
+class InstanceNormWs(InstanceNormLarge):
+    """fnorm_instancenorm_ws (caller workspace): few fp32 slices too long for a
+    cluster take the BatchNorm-kernel route over the [1, N*C, S] view."""
+
+    def __init__(self, dev, shape):
+        super().__init__(dev, shape)
+        self.name = "instancenorm2d_ws_fp32_" + "x".join(str(v) for v in shape)
+        self.nb = fn.fnorm_instancenorm_workspace_size(self.N, self.C, self.S)
+        self.ws = torch.empty(max(self.nb, 1), dtype=torch.uint8, device=dev)
+
+    def step(self, stream):
+        fn.fnorm_instancenorm_ws(self.x, self.y, self.N, self.C, self.S, fn.FNORM_F32,
+                                 fn.FNORM_F32, 1e-5, None, None, self.ws, self.nb, stream)
+
+
 class InstanceNormAffine(InstanceNormLarge):
     """InstanceNorm2d(64, affine=True) on x[112,64,512,512]."""
 
@@ -341,6 +356,8 @@ def make_workload(args, dev) -> Workload:
         return Epilogue(dev, want_arg=True)
     if args.workload == "batchnorm":
         return BatchNorm(dev)
+    if args.workload == "in_ws":
+        return InstanceNormWs(dev, shape or inputs.SHAPE_LARGE)
     if args.workload == "in_affine":
         return InstanceNormAffine(dev, shape or inputs.SHAPE_LARGE)
     if args.workload == "bn_eval":
@@ -685,7 +702,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip e2e, cpu baseline and the other workloads")
     ap.add_argument("--workload", default="in_large",
-                    help="in_large | in_affine | epilogue | epilogue_argmax | batchnorm | bn_eval | "
+                    help="in_large | in_ws | in_affine | epilogue | epilogue_argmax | batchnorm | "
+                         "bn_eval | "
                          "sweep:S[:TOTAL] "
                          "(S a power of 4, 256..4^10; TOTAL elements, default 2^30) | "
                          "floor_read:BYTES | floor_copy:BYTES (torch reference floors)")

@@ -96,6 +96,36 @@ FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int
                                 float* mean_out, float* rstd_out, fnorm_stream_t stream);
 
 /*
+ * fnorm_instancenorm with a caller workspace, for a few slices too long for
+ * one thread-block cluster (more than 2 MiB of fp32 each, e.g. x[1,1,8192,8192]):
+ * without one, each such slice is streamed by a single cluster and most SMs
+ * stay idle. Same arguments, results and errors as fnorm_instancenorm, plus:
+ *
+ *   workspace        device memory of at least
+ *                    fnorm_instancenorm_workspace_size(N, C, S) bytes,
+ *                    256-byte aligned, owned by the caller; its contents need
+ *                    no initialisation and are overwritten. Calls that
+ *                    overlap in time must not share a workspace. It may be
+ *                    NULL when that size is 0.
+ *   workspace_bytes  its size.
+ *
+ * With fp32 input and output, 16-byte aligned x and y, S a multiple of 4, S
+ * above 2^19 and N*C at most a quarter of the SM count, the slices are
+ * normalised as a BatchNorm over the [1, N*C, S] view: a statistics launch
+ * over 64 KiB chunks of every slice (all SMs, per-chunk partials in the
+ * workspace), then an apply launch that merges each slice's partials in a
+ * fixed order (x is read twice, the second time partly from L2). Every other
+ * call takes fnorm_instancenorm's own plan and leaves the workspace untouched.
+ * The results agree with the exact definition to fp32 accuracy on either path.
+ */
+FNORM_API size_t fnorm_instancenorm_workspace_size(int64_t N, int64_t C, int64_t S);
+FNORM_API fnorm_status fnorm_instancenorm_ws(const void* x, void* y, int64_t N, int64_t C,
+                                             int64_t S, fnorm_dtype in_dtype,
+                                             fnorm_dtype out_dtype, float eps, float* mean_out,
+                                             float* rstd_out, void* workspace,
+                                             size_t workspace_bytes, fnorm_stream_t stream);
+
+/*
  * InstanceNorm forward with per-channel affine parameters (the module's
  * affine = True option; Kimi-K2.6__l1_p34, block 2 notes the default is
  * affine = False, and Kimi-K2.6__l2_p73, block 1 states the affine step

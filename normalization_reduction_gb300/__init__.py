@@ -21,6 +21,7 @@ from enum import IntEnum
 __all__ = [
     "FNORM_F32", "FNORM_BF16", "Status", "FnormError", "LIBRARY", "lib",
     "fnorm_instancenorm", "fnorm_instancenorm_affine", "fnorm_instancenorm_epilogue",
+    "fnorm_instancenorm_workspace_size", "fnorm_instancenorm_ws",
     "fnorm_batchnorm_workspace_size", "fnorm_batchnorm_eval",
     "fnorm_batchnorm_train", "fnorm_batchnorm_train_noalloc", "fnorm_batchnorm_local_stats",
     "fnorm_batchnorm_apply_stats", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
@@ -60,6 +61,9 @@ _SIGNATURES = {
     "fnorm_instancenorm": ([_vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _vp, _vp, _vp], _int),
     "fnorm_instancenorm_affine": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _vp,
                                    _vp, _vp], _int),
+    "fnorm_instancenorm_workspace_size": ([_i64, _i64, _i64], ctypes.c_size_t),
+    "fnorm_instancenorm_ws": ([_vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _vp, _vp, _vp,
+                               ctypes.c_size_t, _vp], _int),
     "fnorm_batchnorm_eval": ([_vp, _vp, _vp, _vp, _f32, _vp, _vp, _f32, _i64, _i64, _i64, _vp],
                              _int),
     "fnorm_instancenorm_epilogue": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _f32, _vp],
@@ -133,6 +137,18 @@ def fnorm_instancenorm_affine(x, y, gamma, beta, N, C, S, in_dtype, out_dtype, e
                                            in_dtype, out_dtype, eps, _ptr(mean_out),
                                            _ptr(rstd_out), _stream(stream)),
            "fnorm_instancenorm_affine")
+
+
+def fnorm_instancenorm_workspace_size(N, C, S) -> int:
+    return int(lib().fnorm_instancenorm_workspace_size(N, C, S))
+
+
+def fnorm_instancenorm_ws(x, y, N, C, S, in_dtype, out_dtype, eps, mean_out, rstd_out, workspace,
+                          workspace_bytes, stream=None):
+    _check(lib().fnorm_instancenorm_ws(_ptr(x), _ptr(y), N, C, S, in_dtype, out_dtype, eps,
+                                       _ptr(mean_out), _ptr(rstd_out), _ptr(workspace),
+                                       workspace_bytes, _stream(stream)),
+           "fnorm_instancenorm_ws")
 
 
 def fnorm_instancenorm_epilogue(x, m, y, argmax, N, C, S, eps=1e-5, clamp_lo=-1.0, clamp_hi=1.0,
@@ -247,8 +263,15 @@ def instance_norm(x, eps: float = 1e-5, out_dtype=None, out=None, return_stats: 
     if return_stats:
         mean = torch.empty(N * C, dtype=torch.float32, device=x.device)
         rstd = torch.empty(N * C, dtype=torch.float32, device=x.device)
-    fnorm_instancenorm_affine(x, y, weight, bias, N, C, S, _dtype_code(x.dtype),
-                              _dtype_code(y.dtype), eps, mean, rstd, stream)
+    if weight is None and bias is None:
+        # few slices too long for one cluster take the workspace route
+        nb = fnorm_instancenorm_workspace_size(N, C, S)
+        ws = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
+        fnorm_instancenorm_ws(x, y, N, C, S, _dtype_code(x.dtype), _dtype_code(y.dtype), eps,
+                              mean, rstd, ws, nb, stream)
+    else:
+        fnorm_instancenorm_affine(x, y, weight, bias, N, C, S, _dtype_code(x.dtype),
+                                  _dtype_code(y.dtype), eps, mean, rstd, stream)
     return (y, mean, rstd) if return_stats else y
 
 

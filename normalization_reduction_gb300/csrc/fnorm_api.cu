@@ -500,143 +500,7 @@ const DeviceInfo& device_info() {
 
 }  // namespace fnorm
 
-using namespace fnorm;
-
-extern "C" {
-
-int fnorm_version(void) { return 100; }
-
-void fnorm_tuning_reload(void) { load_knobs(); }
-
-void fnorm_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
-
-const char* fnorm_status_string(fnorm_status s) {
-  switch (s) {
-    case FNORM_OK: return "FNORM_OK";
-    case FNORM_ERR_INVALID_ARG: return "FNORM_ERR_INVALID_ARG";
-    case FNORM_ERR_UNSUPPORTED: return "FNORM_ERR_UNSUPPORTED";
-    case FNORM_ERR_ALIGNMENT: return "FNORM_ERR_ALIGNMENT";
-    case FNORM_ERR_CUDA: return "FNORM_ERR_CUDA";
-    case FNORM_ERR_TIMEOUT: return "FNORM_ERR_TIMEOUT";
-  }
-  return "FNORM_ERR_UNKNOWN";
-}
-
-fnorm_status fnorm_get_last_error(void) {
-  unsigned* w = err_word();
-  if (!w) return FNORM_ERR_CUDA;
-  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_status(cudaErrorUnknown);
-  unsigned v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_fnorm_err_word, sizeof v) != cudaSuccess)
-    return cuda_status(cudaErrorUnknown);
-  const unsigned zero = 0;
-  if (cudaMemcpyToSymbol(g_fnorm_err_word, &zero, sizeof zero) != cudaSuccess)
-    return cuda_status(cudaErrorUnknown);
-  return (v & kErrTimeout) ? FNORM_ERR_TIMEOUT : FNORM_OK;
-}
-
-fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const float* gamma,
-                                       const float* beta, int64_t N, int64_t C, int64_t S,
-                                       fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
-                                       float* mean_out, float* rstd_out, fnorm_stream_t stream) {
-  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
-  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4))) return FNORM_ERR_ALIGNMENT;
-  if ((in_dtype != FNORM_F32 && in_dtype != FNORM_BF16) ||
-      (out_dtype != FNORM_F32 && out_dtype != FNORM_BF16))
-    return FNORM_ERR_INVALID_ARG;
-  if (!finite_nonneg(eps)) return FNORM_ERR_INVALID_ARG;
-  int64_t NC = 0, total = 0;
-  if (!mul_ok(N, C, &NC) || !mul_ok(NC, S, &total)) return FNORM_ERR_INVALID_ARG;
-  if (total == 0) return FNORM_OK;
-  if (!x || !y) return FNORM_ERR_INVALID_ARG;
-  const int tin = in_dtype == FNORM_F32 ? 0 : 1, tout = out_dtype == FNORM_F32 ? 0 : 1;
-  const size_t es_in = tin == 0 ? 4 : 2, es_out = tout == 0 ? 4 : 2;
-  if (!aligned(x, es_in) || !aligned(y, es_out) || (mean_out && !aligned(mean_out, 4)) ||
-      (rstd_out && !aligned(rstd_out, 4)))
-    return FNORM_ERR_ALIGNMENT;
-  const size_t xb = static_cast<size_t>(total) * es_in, yb = static_cast<size_t>(total) * es_out;
-  if (x != y && overlaps(x, xb, y, yb)) return FNORM_ERR_INVALID_ARG;
-  if (x == y && es_in != es_out) return FNORM_ERR_INVALID_ARG;
-  const size_t sb = static_cast<size_t>(NC) * 4;
-  if (overlaps(mean_out, sb, x, xb) || overlaps(mean_out, sb, y, yb) ||
-      overlaps(rstd_out, sb, x, xb) || overlaps(rstd_out, sb, y, yb) ||
-      overlaps(mean_out, sb, rstd_out, sb))
-    return FNORM_ERR_INVALID_ARG;
-  const size_t cb = static_cast<size_t>(C) * 4;
-  if (overlaps(gamma, cb, y, yb) || overlaps(beta, cb, y, yb) || overlaps(gamma, cb, mean_out, sb) ||
-      overlaps(gamma, cb, rstd_out, sb) || overlaps(beta, cb, mean_out, sb) ||
-      overlaps(beta, cb, rstd_out, sb))
-    return FNORM_ERR_INVALID_ARG;
-
-  InPlan plan;
-  fnorm_status st = in_make_plan(tin, tout, x, y, NC, S, &plan);
-  if (st != FNORM_OK) return st;
-  unsigned* err = err_word();
-  if (!err) return FNORM_ERR_CUDA;
-  const InParams p{x,    y,     NC,   S, eps, mean_out, rstd_out, err, gamma, beta, C,
-                   force_timeout()};
-  return cuda_status(in_launch_dispatch(tin, tout, p, plan, reinterpret_cast<cudaStream_t>(stream)));
-}
-
-fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
-                                fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
-                                float* mean_out, float* rstd_out, fnorm_stream_t stream) {
-  return fnorm_instancenorm_affine(x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype, eps,
-                                   mean_out, rstd_out, stream);
-}
-
-fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
-                                         int64_t N, int64_t C, int64_t S, float eps,
-                                         float clamp_lo, float clamp_hi, fnorm_stream_t stream) {
-  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
-  if (!finite_nonneg(eps) || std::isnan(clamp_lo) || std::isnan(clamp_hi) || !(clamp_lo <= clamp_hi))
-    return FNORM_ERR_INVALID_ARG;
-  int64_t NS = 0, NC = 0, total = 0;
-  if (!mul_ok(N, S, &NS) || !mul_ok(N, C, &NC) || !mul_ok(NC, S, &total))
-    return FNORM_ERR_INVALID_ARG;
-  if (NS == 0) return FNORM_OK;
-  if (C == 0) return FNORM_ERR_INVALID_ARG;   // a max over no channels is undefined
-  if (C > kEpiMaxChannels) return FNORM_ERR_UNSUPPORTED;
-  if (!x || !m || !y) return FNORM_ERR_INVALID_ARG;
-  if (!aligned(x, 4) || !aligned(m, 4) || !aligned(y, 4) || (argmax && !aligned(argmax, 8)))
-    return FNORM_ERR_ALIGNMENT;
-  const size_t xb = static_cast<size_t>(total) * 4, yb = static_cast<size_t>(NS) * 4,
-               ab = argmax ? static_cast<size_t>(NS) * 8 : 0, mb = static_cast<size_t>(C) * 4;
-  if (overlaps(y, yb, x, xb) || overlaps(y, yb, m, mb) || overlaps(argmax, ab, x, xb) ||
-      overlaps(argmax, ab, m, mb) || overlaps(argmax, ab, y, yb))
-    return FNORM_ERR_INVALID_ARG;
-
-  EpiPlan plan;
-  fnorm_status st = epi_make_plan(x, y, argmax, N, C, S, &plan);
-  if (st != FNORM_OK) return st;
-  unsigned* err = err_word();
-  if (!err) return FNORM_ERR_CUDA;
-  EpiParams p{};
-  p.x = x;
-  p.m = m;
-  p.y = y;
-  p.argmax = argmax;
-  p.N = N;
-  p.C = C;
-  p.S = S;
-  p.eps = eps;
-  p.lo = clamp_lo;
-  p.hi = clamp_hi;
-  p.per = plan.per;
-  p.debug_timeout = force_timeout();
-  p.keep = plan.keep;
-  p.err = err;
-  return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
-}
-
-size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S) {
-  if (N <= 0 || C <= 0 || S <= 0) return 0;
-  int64_t t1 = 0, t2 = 0;
-  if (!mul_ok(N, C, &t1) || !mul_ok(t1, S, &t2)) return 0;
-  const BnLayout l = bn_layout(N, C, S);
-  return l.ws_bytes;
-}
-
+namespace fnorm {
 namespace {
 
 // Shared validation of the BatchNorm entry points. `need_stats` >= 2: the
@@ -696,6 +560,210 @@ void bn_fill(BnParams* p, const float* x, float* y, const float* gamma, const fl
 }
 
 }  // namespace
+}  // namespace fnorm
+
+namespace fnorm {
+namespace {
+
+// Few fp32 slices too long for one cluster (the stream plan would keep most
+// SMs idle): with a caller workspace, fnorm_instancenorm_ws runs them as a
+// BatchNorm over the [1, N*C, S] view -- the per-(slice, 64 KiB chunk)
+// statistics and apply launches spread every slice over all SMs; a slice's
+// mean and rstd are the BatchNorm channel's saved statistics.
+bool in_ws_shape(int64_t NC, int64_t S) {
+  return S / 4 > int64_t(kMaxCluster) * 8192 && NC * 4 <= device_info().sm_count;
+}
+
+// Validation and launch of the InstanceNorm entry points. `workspace` (may
+// be null) is used only by the route above.
+fnorm_status in_call(const void* x, void* y, const float* gamma, const float* beta, int64_t N,
+                     int64_t C, int64_t S, fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                     float* mean_out, float* rstd_out, void* workspace, size_t workspace_bytes,
+                     fnorm_stream_t stream) {
+  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4))) return FNORM_ERR_ALIGNMENT;
+  if ((in_dtype != FNORM_F32 && in_dtype != FNORM_BF16) ||
+      (out_dtype != FNORM_F32 && out_dtype != FNORM_BF16))
+    return FNORM_ERR_INVALID_ARG;
+  if (!finite_nonneg(eps)) return FNORM_ERR_INVALID_ARG;
+  int64_t NC = 0, total = 0;
+  if (!mul_ok(N, C, &NC) || !mul_ok(NC, S, &total)) return FNORM_ERR_INVALID_ARG;
+  if (total == 0) return FNORM_OK;
+  if (!x || !y) return FNORM_ERR_INVALID_ARG;
+  const int tin = in_dtype == FNORM_F32 ? 0 : 1, tout = out_dtype == FNORM_F32 ? 0 : 1;
+  const size_t es_in = tin == 0 ? 4 : 2, es_out = tout == 0 ? 4 : 2;
+  if (!aligned(x, es_in) || !aligned(y, es_out) || (mean_out && !aligned(mean_out, 4)) ||
+      (rstd_out && !aligned(rstd_out, 4)))
+    return FNORM_ERR_ALIGNMENT;
+  const size_t xb = static_cast<size_t>(total) * es_in, yb = static_cast<size_t>(total) * es_out;
+  if (x != y && overlaps(x, xb, y, yb)) return FNORM_ERR_INVALID_ARG;
+  if (x == y && es_in != es_out) return FNORM_ERR_INVALID_ARG;
+  const size_t sb = static_cast<size_t>(NC) * 4;
+  if (overlaps(mean_out, sb, x, xb) || overlaps(mean_out, sb, y, yb) ||
+      overlaps(rstd_out, sb, x, xb) || overlaps(rstd_out, sb, y, yb) ||
+      overlaps(mean_out, sb, rstd_out, sb))
+    return FNORM_ERR_INVALID_ARG;
+  const size_t cb = static_cast<size_t>(C) * 4;
+  if (overlaps(gamma, cb, y, yb) || overlaps(beta, cb, y, yb) || overlaps(gamma, cb, mean_out, sb) ||
+      overlaps(gamma, cb, rstd_out, sb) || overlaps(beta, cb, mean_out, sb) ||
+      overlaps(beta, cb, rstd_out, sb))
+    return FNORM_ERR_INVALID_ARG;
+
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (workspace && tin == 0 && tout == 0 && !gamma && !beta && in_ws_shape(NC, S) &&
+      aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_PATH") &&
+      !env("FNORM_FORCE_SCALAR")) {
+    const BnLayout l = bn_layout(1, NC, S);
+    if (!aligned(workspace, 256)) return FNORM_ERR_ALIGNMENT;
+    if (workspace_bytes < l.ws_bytes) return FNORM_ERR_INVALID_ARG;
+    if (overlaps(workspace, l.ws_bytes, x, xb) || overlaps(workspace, l.ws_bytes, y, yb) ||
+        overlaps(workspace, l.ws_bytes, mean_out, sb) ||
+        overlaps(workspace, l.ws_bytes, rstd_out, sb))
+      return FNORM_ERR_INVALID_ARG;
+    unsigned* err = err_word();
+    if (!err) return FNORM_ERR_CUDA;
+    BnParams p{};
+    bn_fill(&p, static_cast<const float*>(x), static_cast<float*>(y), nullptr, nullptr, 1.f,
+            nullptr, nullptr, 0.f, eps, mean_out, rstd_out, 1, NC, S, err);
+    p.partials = static_cast<float4*>(workspace);
+    p.stats = p.partials;
+    p.stats_cstride = l.P;
+    p.stats_istride = 1;
+    p.stats_count = l.P;
+    p.grid_counter = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + l.ws_bytes - 256);
+    if (p.vec && p.split) return cuda_status(bn_launch(p, cs));
+  }
+
+  InPlan plan;
+  fnorm_status st = in_make_plan(tin, tout, x, y, NC, S, &plan);
+  if (st != FNORM_OK) return st;
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  const InParams p{x,    y,     NC,   S, eps, mean_out, rstd_out, err, gamma, beta, C,
+                   force_timeout()};
+  return cuda_status(in_launch_dispatch(tin, tout, p, plan, cs));
+}
+
+}  // namespace
+}  // namespace fnorm
+
+using namespace fnorm;
+
+extern "C" {
+
+int fnorm_version(void) { return 100; }
+
+void fnorm_tuning_reload(void) { load_knobs(); }
+
+void fnorm_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
+
+const char* fnorm_status_string(fnorm_status s) {
+  switch (s) {
+    case FNORM_OK: return "FNORM_OK";
+    case FNORM_ERR_INVALID_ARG: return "FNORM_ERR_INVALID_ARG";
+    case FNORM_ERR_UNSUPPORTED: return "FNORM_ERR_UNSUPPORTED";
+    case FNORM_ERR_ALIGNMENT: return "FNORM_ERR_ALIGNMENT";
+    case FNORM_ERR_CUDA: return "FNORM_ERR_CUDA";
+    case FNORM_ERR_TIMEOUT: return "FNORM_ERR_TIMEOUT";
+  }
+  return "FNORM_ERR_UNKNOWN";
+}
+
+fnorm_status fnorm_get_last_error(void) {
+  unsigned* w = err_word();
+  if (!w) return FNORM_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fnorm_err_word, sizeof v) != cudaSuccess)
+    return cuda_status(cudaErrorUnknown);
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_fnorm_err_word, &zero, sizeof zero) != cudaSuccess)
+    return cuda_status(cudaErrorUnknown);
+  return (v & kErrTimeout) ? FNORM_ERR_TIMEOUT : FNORM_OK;
+}
+
+fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const float* gamma,
+                                       const float* beta, int64_t N, int64_t C, int64_t S,
+                                       fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                       float* mean_out, float* rstd_out, fnorm_stream_t stream) {
+  return in_call(x, y, gamma, beta, N, C, S, in_dtype, out_dtype, eps, mean_out, rstd_out, nullptr,
+                 0, stream);
+}
+
+fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
+                                fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                float* mean_out, float* rstd_out, fnorm_stream_t stream) {
+  return in_call(x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype, eps, mean_out, rstd_out,
+                 nullptr, 0, stream);
+}
+
+size_t fnorm_instancenorm_workspace_size(int64_t N, int64_t C, int64_t S) {
+  int64_t NC = 0, total = 0;
+  if (N <= 0 || C <= 0 || S <= 0 || !mul_ok(N, C, &NC) || !mul_ok(NC, S, &total)) return 0;
+  if (!in_ws_shape(NC, S)) return 0;
+  return bn_layout(1, NC, S).ws_bytes;
+}
+
+fnorm_status fnorm_instancenorm_ws(const void* x, void* y, int64_t N, int64_t C, int64_t S,
+                                   fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
+                                   float* mean_out, float* rstd_out, void* workspace,
+                                   size_t workspace_bytes, fnorm_stream_t stream) {
+  return in_call(x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype, eps, mean_out, rstd_out,
+                 workspace, workspace_bytes, stream);
+}
+
+fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
+                                         int64_t N, int64_t C, int64_t S, float eps,
+                                         float clamp_lo, float clamp_hi, fnorm_stream_t stream) {
+  if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
+  if (!finite_nonneg(eps) || std::isnan(clamp_lo) || std::isnan(clamp_hi) || !(clamp_lo <= clamp_hi))
+    return FNORM_ERR_INVALID_ARG;
+  int64_t NS = 0, NC = 0, total = 0;
+  if (!mul_ok(N, S, &NS) || !mul_ok(N, C, &NC) || !mul_ok(NC, S, &total))
+    return FNORM_ERR_INVALID_ARG;
+  if (NS == 0) return FNORM_OK;
+  if (C == 0) return FNORM_ERR_INVALID_ARG;   // a max over no channels is undefined
+  if (C > kEpiMaxChannels) return FNORM_ERR_UNSUPPORTED;
+  if (!x || !m || !y) return FNORM_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(m, 4) || !aligned(y, 4) || (argmax && !aligned(argmax, 8)))
+    return FNORM_ERR_ALIGNMENT;
+  const size_t xb = static_cast<size_t>(total) * 4, yb = static_cast<size_t>(NS) * 4,
+               ab = argmax ? static_cast<size_t>(NS) * 8 : 0, mb = static_cast<size_t>(C) * 4;
+  if (overlaps(y, yb, x, xb) || overlaps(y, yb, m, mb) || overlaps(argmax, ab, x, xb) ||
+      overlaps(argmax, ab, m, mb) || overlaps(argmax, ab, y, yb))
+    return FNORM_ERR_INVALID_ARG;
+
+  EpiPlan plan;
+  fnorm_status st = epi_make_plan(x, y, argmax, N, C, S, &plan);
+  if (st != FNORM_OK) return st;
+  unsigned* err = err_word();
+  if (!err) return FNORM_ERR_CUDA;
+  EpiParams p{};
+  p.x = x;
+  p.m = m;
+  p.y = y;
+  p.argmax = argmax;
+  p.N = N;
+  p.C = C;
+  p.S = S;
+  p.eps = eps;
+  p.lo = clamp_lo;
+  p.hi = clamp_hi;
+  p.per = plan.per;
+  p.debug_timeout = force_timeout();
+  p.keep = plan.keep;
+  p.err = err;
+  return cuda_status(epi_launch(p, plan, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t fnorm_batchnorm_workspace_size(int64_t N, int64_t C, int64_t S) {
+  if (N <= 0 || C <= 0 || S <= 0) return 0;
+  int64_t t1 = 0, t2 = 0;
+  if (!mul_ok(N, C, &t1) || !mul_ok(t1, S, &t2)) return 0;
+  const BnLayout l = bn_layout(N, C, S);
+  return l.ws_bytes;
+}
+
 
 }  // extern "C"
 

@@ -55,6 +55,24 @@ def test_tuning_switches_read_once(lib, monkeypatch):
     assert src.count("std::getenv(") == 1   # only the one-time reader
 
 
+def test_instancenorm_ws_validation(lib):
+    """The workspace entry point validates like fnorm_instancenorm; its size is
+    0 for shapes that do not take the workspace route."""
+    assert fn.fnorm_instancenorm_workspace_size(112, 64, 512 * 512) == 0   # fits a cluster
+    assert fn.fnorm_instancenorm_workspace_size(0, 1, 1 << 26) == 0
+    assert fn.fnorm_instancenorm_workspace_size(1, 1, -1) == 0
+    a = dict(x=FAKE, y=FAKE + (1 << 30), N=2, C=3, S=64, in_dtype=fn.FNORM_F32,
+             out_dtype=fn.FNORM_F32, eps=1e-5, mean_out=None, rstd_out=None, workspace=None,
+             workspace_bytes=0, stream=0)
+    for kw, expect in [(dict(N=-1), fn.Status.ERR_INVALID_ARG),
+                       (dict(eps=-1.0), fn.Status.ERR_INVALID_ARG),
+                       (dict(x=FAKE + 2), fn.Status.ERR_ALIGNMENT),
+                       (dict(N=0), fn.Status.OK)]:
+        b = dict(a)
+        b.update(kw)
+        assert _rc(lambda: fn.fnorm_instancenorm_ws(**b)) == expect, kw
+
+
 def test_status_strings_and_version(lib):
     for s in fn.Status:
         assert fn.fnorm_status_string(int(s)) == "FNORM_" + s.name
@@ -222,6 +240,8 @@ int call_all(void* x, void* y, float* g, float* m, long long* a, void* ws, fnorm
                                    1e-5f, 0, 0, 2, 3, 64, s);
   st = fnorm_batchnorm_train_noalloc((const float*)x, (float*)y, g, g, 2.f, g, g, 0.1f, 1e-5f,
                                      0, 0, 2, 3, 64, s);
+  size_t iw = fnorm_instancenorm_workspace_size(1, 1, 1 << 26);
+  st = fnorm_instancenorm_ws(x, y, 2, 3, 64, FNORM_F32, FNORM_F32, 1e-5f, 0, 0, ws, iw, s);
   fnorm_tuning_reload();
   fnorm_debug_force_timeout(0);
   printf("%s %d %d\n", fnorm_status_string(st), (int)fnorm_get_last_error(), fnorm_version());

@@ -302,3 +302,45 @@ def test_bf16_packed_outliers_at_thread_shifts(orc, S, threads, chunk):
     ref, rmean, rvar = oracle_in(orc, x)
     assert_close(to_f64(y), ref, torch.float32, f"thread-shift outliers S={S}")
     assert np.allclose(rs.cpu().numpy()[:NC], 1 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)
+
+
+@pytest.mark.parametrize("shape,dtype", [
+    ((1, 1, 4096, 4100), torch.float32),   # one slice of 16.8 M values: the workspace route
+    ((1, 3, 2048, 2048), torch.float32),
+    ((8, 3, 1024, 1024), torch.float32),   # 24 slices
+    ((1, 1, 2048, 2050), torch.bfloat16),  # bf16 keeps fnorm_instancenorm's plan
+    ((2, 3, 64, 64), torch.float32),       # fits a cluster: fnorm_instancenorm's plan
+])
+def test_workspace_entry_point(orc, shape, dtype):
+    """fnorm_instancenorm_ws against the oracle, element by element, with the
+    mean and rstd outputs, on shapes that take its workspace route (few fp32
+    slices longer than a cluster holds) and shapes that do not; the workspace
+    starts dirty."""
+    N, C = shape[0], shape[1]
+    S = int(np.prod(shape[2:]))
+    x = inputs.normal((N, C, S), 1301 + C, dev(), mean=1.5, std=2.0, dtype=dtype)
+    y = torch.empty_like(x)
+    mean = torch.empty(N * C, device=dev())
+    rstd = torch.empty(N * C, device=dev())
+    nb = fn.fnorm_instancenorm_workspace_size(N, C, S)
+    ws = torch.full((max(nb, 1),), 0xA5, dtype=torch.uint8, device=dev())
+    code = fn.FNORM_F32 if dtype == torch.float32 else fn.FNORM_BF16
+    fn.fnorm_instancenorm_ws(x, y, N, C, S, code, code, EPS, mean, rstd, ws, nb)
+    torch.cuda.synchronize()
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    if dtype == torch.float32:
+        ref, rmean, rvar = orc.instancenorm(x.cpu().numpy().reshape(N * C, S), EPS)
+        assert_close(y.cpu().numpy().reshape(N * C, S), ref, torch.float32, f"ws {shape}")
+    else:
+        xb = x.view(torch.int16).cpu().numpy().view(np.uint16).reshape(N * C, S)
+        ref_bits, rmean, rvar = orc.instancenorm(xb, EPS)
+        yb = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(N * C, S)
+        to64 = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        assert_close(to64(yb), to64(ref_bits), torch.bfloat16, f"ws {shape}")
+    assert np.max(np.abs(mean.cpu().numpy() - rmean)) <= 1e-5
+    assert np.allclose(rstd.cpu().numpy(), 1 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)
+    if shape == (1, 1, 4096, 4100):
+        assert nb > 0
+        with pytest.raises(fn.FnormError) as e:   # too small a workspace
+            fn.fnorm_instancenorm_ws(x, y, N, C, S, code, code, EPS, None, None, ws, nb - 256)
+        assert e.value.status == fn.Status.ERR_INVALID_ARG
