@@ -128,3 +128,32 @@ def test_fuzz_batchnorm(orc, case):
         assert_close(y.cpu().numpy(), ref, torch.float32, what)
         assert np.max(np.abs(rm.cpu().numpy() - rmo)) <= 1e-6, what
         assert np.max(np.abs(rv.cpu().numpy() - rvo)) <= 2e-6, what
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_fuzz_instancenorm_workspace(orc, case):
+    """fnorm_instancenorm_ws with few long fp32 slices (the workspace route when
+    aligned), random lengths around and above a cluster's capacity, sometimes
+    misaligned (then the regular plan), with the mean and rstd outputs."""
+    rng = np.random.default_rng(9700 + case)
+    S = int(rng.integers(1 << 19, 3 << 20))
+    if rng.random() < 0.7:
+        S -= S % 4
+    NC = int(rng.integers(1, 5))
+    misalign = rng.random() < 0.25
+    xb = inputs.normal((NC * S + 1,), 9700 + case, dev(), mean=-2.0, std=0.5)
+    x = xb[1:] if misalign else xb[:NC * S]
+    y = Guarded((NC * S,), torch.float32, offset_elems=1 if misalign else 0)
+    mean = torch.empty(NC, device=dev())
+    rstd = torch.empty(NC, device=dev())
+    nb = fn.fnorm_instancenorm_workspace_size(1, NC, S)
+    ws = torch.full((max(nb, 1),), 0x3C, dtype=torch.uint8, device=dev())
+    fn.fnorm_instancenorm_ws(x, y.view, 1, NC, S, fn.FNORM_F32, fn.FNORM_F32, EPS, mean, rstd, ws,
+                             nb)
+    torch.cuda.synchronize()
+    y.check()
+    ref, rmean, rvar = orc.instancenorm(x.cpu().numpy().reshape(NC, S), EPS)
+    assert_close(y.view.cpu().numpy().reshape(NC, S), ref, torch.float32,
+                 f"ws case {case} NC={NC} S={S} misalign={misalign}")
+    assert np.max(np.abs(mean.cpu().numpy() - rmean)) <= 1e-5
+    assert np.allclose(rstd.cpu().numpy(), 1 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)

@@ -104,3 +104,23 @@ def test_first_calls_inside_capture():
     r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and "fresh ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
+
+
+def test_graph_instancenorm_workspace_route():
+    """fnorm_instancenorm_ws on a shape that takes its workspace route (two
+    BatchNorm-kernel launches on the caller's stream) and on one that does not."""
+    ys, runs = [], []
+    for shape in ((1, 2, 1 << 20), (2, 3, 4096)):
+        N, C, S = shape
+        x = inputs.normal(shape, 17 + C, dev())
+        y = torch.empty_like(x)
+        nb = fn.fnorm_instancenorm_workspace_size(N, C, S)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev())
+        ys.append(y)
+        runs.append((x, y, ws, nb, N, C, S))
+
+    def run():
+        for x, y, ws, nb, N, C, S in runs:
+            fn.fnorm_instancenorm_ws(x, y, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None,
+                                     ws, nb, torch.cuda.current_stream())
+    _capture_and_compare(run, ys)
