@@ -110,7 +110,8 @@ FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int
  *   workspace_bytes  its size.
  *
  * With fp32 input and output, 16-byte aligned x and y, S a multiple of 4, S
- * above 2^19 and N*C at most a quarter of the SM count, the slices are
+ * above 2^19 and N*C at most a quarter of the current device's SM count (the
+ * workspace size is likewise that of the current device), the slices are
  * normalised as a BatchNorm over the [1, N*C, S] view: a statistics launch
  * over 64 KiB chunks of every slice (all SMs, per-chunk partials in the
  * workspace), then an apply launch that merges each slice's partials in a
