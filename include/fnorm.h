@@ -114,8 +114,10 @@ FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int
  * workspace size is likewise that of the current device), the slices are
  * normalised as a BatchNorm over the [1, N*C, S] view: a statistics launch
  * over 64 KiB chunks of every slice (all SMs, per-chunk partials in the
- * workspace), then an apply launch that merges each slice's partials in a
- * fixed order (x is read twice, the second time partly from L2). Every other
+ * workspace), for slices of 16 Mi values or more a launch that merges each
+ * slice's partials, and an apply launch that merges them (or takes the merged
+ * value) in a fixed order and normalises (x is read twice, the second time
+ * partly from L2). Every other
  * call takes fnorm_instancenorm's own plan and leaves the workspace untouched.
  * The results agree with the exact definition to fp32 accuracy on either path.
  */
