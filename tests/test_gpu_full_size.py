@@ -18,6 +18,8 @@ host cores (tests/gpu_util.check_in_chunks):
 * Affine InstanceNorm fp32 x[112,64,512,512]: every slice.
 * Eval BatchNorm fp32 x[128,64,126,126]: every sample.
 * InstanceNorm fp32 x[132,64,512,512] (more than 2^31 elements): every slice.
+* fnorm_instancenorm_ws on x[1,1,8192,8192] (one slice of 67 M values).
+* fnorm_instancenorm_ws on x[1,1,8192,8192] (one slice of 67 M values).
 * Counts above 2^24 that are not powers of two (the statistics carry fp32
   counts): InstanceNorm slices of 4097 x 4097 and 4096 x 4100 values, and
   BatchNorm channels of 3 * 2^23 + 5 and 3 * (2^23 + 4) values, on the
@@ -259,3 +261,23 @@ def test_batchnorm_count_above_2e24(orc, N, S):
     assert np.max(np.abs(rv.cpu().numpy() - rvo)) <= 2e-6
     assert np.max(np.abs(sm.cpu().numpy() - mean)) <= 1e-5
     assert np.allclose(sr.cpu().numpy(), 1 / np.sqrt(var + EPS), rtol=2e-6, atol=0)
+
+
+def test_instancenorm_workspace_route_largest_slice(orc):
+    """fnorm_instancenorm_ws on x[1,1,8192,8192] fp32 (one slice of 67 M
+    values: the chunked statistics, the per-slice merge launch and the apply
+    pass), every element and the mean/rstd outputs against the oracle."""
+    N, C, S = 1, 1, 8192 * 8192
+    x = inputs.normal((N, C, S), 1401, dev(), mean=0.25, std=3.0)
+    y = torch.empty_like(x)
+    mean = torch.empty(1, device=dev())
+    rstd = torch.empty(1, device=dev())
+    nb = fn.fnorm_instancenorm_workspace_size(N, C, S)
+    assert nb > 0
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev())
+    fn.fnorm_instancenorm_ws(x, y, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, mean, rstd, ws, nb)
+    torch.cuda.synchronize()
+    check_instancenorm_all_slices(orc, x.view(1, S), y.view(1, S), mean, rstd, "ws 8192^2",
+                                  chunk=1)
+    del x, y
+    torch.cuda.empty_cache()
