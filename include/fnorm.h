@@ -346,6 +346,17 @@ FNORM_API int fnorm_version(void);
 FNORM_API void fnorm_tuning_reload(void);
 FNORM_API void fnorm_debug_force_timeout(int on);
 
+/*
+ * fnorm_debug_fail_launches(n): the next n calls of the computing entry
+ * points that pass their argument checks return FNORM_ERR_CUDA without
+ * launching anything, as a failed launch would (outputs untouched). n <= 0
+ * clears it. It exists to test callers' error paths; nothing else sets it.
+ *
+ * Every computing entry point also opens an NVTX range named after itself
+ * around its planning and launches, for profilers that collect NVTX.
+ */
+FNORM_API void fnorm_debug_fail_launches(int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ __all__ = [
     "fnorm_batchnorm_workspace_size", "fnorm_batchnorm_eval",
     "fnorm_batchnorm_train", "fnorm_batchnorm_train_noalloc", "fnorm_batchnorm_local_stats",
     "fnorm_batchnorm_apply_stats", "fnorm_status_string", "fnorm_get_last_error", "fnorm_version",
-    "fnorm_tuning_reload", "fnorm_debug_force_timeout",
+    "fnorm_tuning_reload", "fnorm_debug_force_timeout", "fnorm_debug_fail_launches",
     "instance_norm", "instance_norm_epilogue", "batch_norm_train", "batch_norm_eval",
 ]
 
@@ -81,6 +81,7 @@ _SIGNATURES = {
     "fnorm_version": ([], _int),
     "fnorm_tuning_reload": ([], None),
     "fnorm_debug_force_timeout": ([_int], None),
+    "fnorm_debug_fail_launches": ([_int], None),
 }
 
 
@@ -223,6 +224,12 @@ def fnorm_tuning_reload() -> None:
     """Re-reads the FNORM_* tuning switches from the environment (tests and
     experiments; the library reads them once per process otherwise)."""
     lib().fnorm_tuning_reload()
+
+
+def fnorm_debug_fail_launches(n: int) -> None:
+    """Test hook: the next n computing calls that pass their argument checks
+    return FNORM_ERR_CUDA without launching; 0 clears it."""
+    lib().fnorm_debug_fail_launches(int(n))
 
 
 def fnorm_debug_force_timeout(on: bool) -> None:

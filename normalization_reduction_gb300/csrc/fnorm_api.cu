@@ -14,6 +14,8 @@
 #include <mutex>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/fnorm.h"
 #include "fnorm_internal.h"
 
@@ -125,6 +127,27 @@ const char* env(const char* name) {
 // barrier that nothing completes, so that its bounded wait expires.
 std::atomic<int> g_force_timeout{0};
 int force_timeout() { return g_force_timeout.load(std::memory_order_relaxed) ? 1 : 0; }
+
+// Test hook (fnorm_debug_fail_launches): the next n calls that pass their
+// argument checks return FNORM_ERR_CUDA instead of launching, as a failed
+// launch would. Each call consumes one.
+std::atomic<int> g_fail_launches{0};
+bool injected_launch_failure() {
+  int n = g_fail_launches.load(std::memory_order_relaxed);
+  while (n > 0) {
+    if (g_fail_launches.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return true;
+  }
+  return false;
+}
+
+// An NVTX range named after the entry point around the planning and launches
+// of one call (visible to profilers that collect NVTX; nearly free otherwise).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 int occupancy_cached(const std::string& key, int (*query)(const void*), const void* arg) {
   const int d = current_device();
@@ -584,10 +607,10 @@ size_t in_ws_bytes(int64_t NC, int64_t S) {
 
 // Validation and launch of the InstanceNorm entry points. `workspace` (may
 // be null) is used only by the route above.
-fnorm_status in_call(const void* x, void* y, const float* gamma, const float* beta, int64_t N,
-                     int64_t C, int64_t S, fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
-                     float* mean_out, float* rstd_out, void* workspace, size_t workspace_bytes,
-                     fnorm_stream_t stream) {
+fnorm_status in_call(const char* name, const void* x, void* y, const float* gamma,
+                     const float* beta, int64_t N, int64_t C, int64_t S, fnorm_dtype in_dtype,
+                     fnorm_dtype out_dtype, float eps, float* mean_out, float* rstd_out,
+                     void* workspace, size_t workspace_bytes, fnorm_stream_t stream) {
   if (N < 0 || C < 0 || S < 0) return FNORM_ERR_INVALID_ARG;
   if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4))) return FNORM_ERR_ALIGNMENT;
   if ((in_dtype != FNORM_F32 && in_dtype != FNORM_BF16) ||
@@ -617,6 +640,8 @@ fnorm_status in_call(const void* x, void* y, const float* gamma, const float* be
       overlaps(beta, cb, rstd_out, sb))
     return FNORM_ERR_INVALID_ARG;
 
+  const CallRange range(name);
+  if (injected_launch_failure()) return FNORM_ERR_CUDA;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (workspace && tin == 0 && tout == 0 && !gamma && !beta && in_ws_shape(NC, S) &&
       aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_PATH") &&
@@ -679,6 +704,8 @@ void fnorm_tuning_reload(void) { load_knobs(); }
 
 void fnorm_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
 
+void fnorm_debug_fail_launches(int n) { g_fail_launches.store(n > 0 ? n : 0); }
+
 const char* fnorm_status_string(fnorm_status s) {
   switch (s) {
     case FNORM_OK: return "FNORM_OK";
@@ -708,15 +735,15 @@ fnorm_status fnorm_instancenorm_affine(const void* x, void* y, const float* gamm
                                        const float* beta, int64_t N, int64_t C, int64_t S,
                                        fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
                                        float* mean_out, float* rstd_out, fnorm_stream_t stream) {
-  return in_call(x, y, gamma, beta, N, C, S, in_dtype, out_dtype, eps, mean_out, rstd_out, nullptr,
-                 0, stream);
+  return in_call("fnorm_instancenorm_affine", x, y, gamma, beta, N, C, S, in_dtype, out_dtype, eps,
+                 mean_out, rstd_out, nullptr, 0, stream);
 }
 
 fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int64_t C, int64_t S,
                                 fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
                                 float* mean_out, float* rstd_out, fnorm_stream_t stream) {
-  return in_call(x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype, eps, mean_out, rstd_out,
-                 nullptr, 0, stream);
+  return in_call("fnorm_instancenorm", x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype, eps,
+                 mean_out, rstd_out, nullptr, 0, stream);
 }
 
 size_t fnorm_instancenorm_workspace_size(int64_t N, int64_t C, int64_t S) {
@@ -730,8 +757,8 @@ fnorm_status fnorm_instancenorm_ws(const void* x, void* y, int64_t N, int64_t C,
                                    fnorm_dtype in_dtype, fnorm_dtype out_dtype, float eps,
                                    float* mean_out, float* rstd_out, void* workspace,
                                    size_t workspace_bytes, fnorm_stream_t stream) {
-  return in_call(x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype, eps, mean_out, rstd_out,
-                 workspace, workspace_bytes, stream);
+  return in_call("fnorm_instancenorm_ws", x, y, nullptr, nullptr, N, C, S, in_dtype, out_dtype,
+                 eps, mean_out, rstd_out, workspace, workspace_bytes, stream);
 }
 
 fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* y, int64_t* argmax,
@@ -755,6 +782,8 @@ fnorm_status fnorm_instancenorm_epilogue(const float* x, const float* m, float* 
       overlaps(argmax, ab, m, mb) || overlaps(argmax, ab, y, yb))
     return FNORM_ERR_INVALID_ARG;
 
+  const CallRange range("fnorm_instancenorm_epilogue");
+  if (injected_launch_failure()) return FNORM_ERR_CUDA;
   EpiPlan plan;
   fnorm_status st = epi_make_plan(x, y, argmax, N, C, S, &plan);
   if (st != FNORM_OK) return st;
@@ -833,6 +862,8 @@ fnorm_status fnorm_batchnorm_train(const float* x, float* y, const float* gamma,
     if (overlaps(o, cb, workspace, wb)) return FNORM_ERR_INVALID_ARG;
   if (overlaps(workspace, wb, x, xb) || overlaps(workspace, wb, y, xb)) return FNORM_ERR_INVALID_ARG;
 
+  const CallRange range("fnorm_batchnorm_train");
+  if (injected_launch_failure()) return FNORM_ERR_CUDA;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
   BnParams p{};
@@ -869,6 +900,8 @@ fnorm_status fnorm_batchnorm_eval(const float* x, float* y, const float* gamma, 
   if (!y) return FNORM_ERR_INVALID_ARG;
   const BnLayout l = bn_layout(N, C, S);
   if (S >= kBnEvalFlatBelow && l.P > 0x7fffffffLL) return FNORM_ERR_UNSUPPORTED;
+  const CallRange range("fnorm_batchnorm_eval");
+  if (injected_launch_failure()) return FNORM_ERR_CUDA;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
   BnParams p{};
@@ -902,6 +935,8 @@ fnorm_status fnorm_batchnorm_local_stats(const float* x, float* stats_out, int64
   if (overlaps(stats_out, sb, x, xb) || overlaps(stats_out, sb, workspace, l.ws_bytes) ||
       overlaps(workspace, l.ws_bytes, x, xb))
     return FNORM_ERR_INVALID_ARG;
+  const CallRange range("fnorm_batchnorm_local_stats");
+  if (injected_launch_failure()) return FNORM_ERR_CUDA;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
   BnParams p{};
@@ -940,6 +975,8 @@ fnorm_status fnorm_batchnorm_apply_stats(const float* x, float* y, const float* 
   if (!mul_ok(R, C, &RC)) return FNORM_ERR_INVALID_ARG;
   const size_t xb = static_cast<size_t>(total) * 4, sb = static_cast<size_t>(RC) * 16;
   if (overlaps(stats_all, sb, y, xb)) return FNORM_ERR_INVALID_ARG;
+  const CallRange range("fnorm_batchnorm_apply_stats");
+  if (injected_launch_failure()) return FNORM_ERR_CUDA;
   unsigned* err = err_word();
   if (!err) return FNORM_ERR_CUDA;
   BnParams p{};

@@ -73,6 +73,24 @@ def test_instancenorm_ws_validation(lib):
         assert _rc(lambda: fn.fnorm_instancenorm_ws(**b)) == expect, kw
 
 
+def test_injected_launch_failures(lib):
+    """fnorm_debug_fail_launches(n): the next n calls that pass their checks
+    return FNORM_ERR_CUDA before touching the GPU (fake pointers here); calls
+    that fail their checks or are no-ops do not consume one."""
+    a = dict(x=FAKE, y=FAKE + (1 << 30), N=2, C=3, S=64, in_dtype=fn.FNORM_F32,
+             out_dtype=fn.FNORM_F32, eps=1e-5, mean_out=None, rstd_out=None, stream=0)
+    fn.fnorm_debug_fail_launches(2)
+    try:
+        assert _rc(lambda: fn.fnorm_instancenorm(**dict(a, eps=-1.0))) == fn.Status.ERR_INVALID_ARG
+        assert _rc(lambda: fn.fnorm_instancenorm(**dict(a, N=0))) == fn.Status.OK
+        assert _rc(lambda: fn.fnorm_instancenorm(**a)) == fn.Status.ERR_CUDA
+        assert _rc(lambda: fn.fnorm_instancenorm_epilogue(FAKE, FAKE + (1 << 31),
+                                                          FAKE + (1 << 30), None, 2, 3, 64,
+                                                          stream=0)) == fn.Status.ERR_CUDA
+    finally:
+        fn.fnorm_debug_fail_launches(0)
+
+
 def test_status_strings_and_version(lib):
     for s in fn.Status:
         assert fn.fnorm_status_string(int(s)) == "FNORM_" + s.name
@@ -244,6 +262,7 @@ int call_all(void* x, void* y, float* g, float* m, long long* a, void* ws, fnorm
   st = fnorm_instancenorm_ws(x, y, 2, 3, 64, FNORM_F32, FNORM_F32, 1e-5f, 0, 0, ws, iw, s);
   fnorm_tuning_reload();
   fnorm_debug_force_timeout(0);
+  fnorm_debug_fail_launches(0);
   printf("%s %d %d\n", fnorm_status_string(st), (int)fnorm_get_last_error(), fnorm_version());
   return (int)st;
 }

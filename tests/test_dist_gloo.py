@@ -131,3 +131,31 @@ def test_syncbn_exchange_gloo(tmp_path):
         assert acc[0] == sum(splits) * 50
         assert abs(acc[1] - mean[c]) <= 1e-6 * max(1.0, abs(mean[c]))
         assert abs(acc[2] / acc[0] - var[c]) <= 1e-5 * var[c]
+
+
+def _dead_peer_worker(rank, size, port, outdir):
+    import datetime
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    tdist.init_process_group("gloo", rank=rank, world_size=size,
+                             timeout=datetime.timedelta(seconds=5))
+    from normalization_reduction_gb300 import syncbn
+    if rank == 1:
+        return                      # leaves without joining the gather
+    t0 = time.monotonic()
+    try:
+        syncbn.gather_rank_stats(torch.zeros((4, syncbn.STAT_WIDTH)))
+        outcome = "returned"
+    except Exception as e:          # the gather must fail, not hang
+        outcome = "raised " + type(e).__name__
+    with open(os.path.join(outdir, "outcome.txt"), "w") as f:
+        f.write(f"{outcome} {time.monotonic() - t0:.1f}")
+
+
+def test_gather_fails_when_a_rank_leaves(tmp_path):
+    """A rank that leaves before the statistics exchange: the other rank's
+    gather raises within the process-group timeout instead of hanging."""
+    mp.spawn(_dead_peer_worker, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    outcome, secs = open(tmp_path / "outcome.txt").read().rsplit(" ", 1)
+    assert outcome.startswith("raised"), outcome
+    assert float(secs) < 60

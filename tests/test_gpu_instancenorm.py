@@ -344,3 +344,25 @@ def test_workspace_entry_point(orc, shape, dtype):
         with pytest.raises(fn.FnormError) as e:   # too small a workspace
             fn.fnorm_instancenorm_ws(x, y, N, C, S, code, code, EPS, None, None, ws, nb - 256)
         assert e.value.status == fn.Status.ERR_INVALID_ARG
+
+
+def test_injected_launch_failure_leaves_outputs_untouched(orc):
+    """A call failed by fnorm_debug_fail_launches raises FNORM_ERR_CUDA and
+    writes nothing; the next call runs normally."""
+    x = inputs.normal((3, 4, 1000), 1501, dev())
+    g = Guarded((3, 4, 1000), torch.float32)
+    fn.fnorm_debug_fail_launches(1)
+    try:
+        with pytest.raises(fn.FnormError) as e:
+            fn.fnorm_instancenorm(x, g.view, 3, 4, 1000, fn.FNORM_F32, fn.FNORM_F32, EPS, None,
+                                  None)
+        assert e.value.status == fn.Status.ERR_CUDA
+        torch.cuda.synchronize()
+        assert bool((g.buf == g.buf[0]).all())          # canary value everywhere
+        fn.fnorm_instancenorm(x, g.view, 3, 4, 1000, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None)
+        torch.cuda.synchronize()
+    finally:
+        fn.fnorm_debug_fail_launches(0)
+    g.check()
+    ref, _, _ = orc.instancenorm(x.cpu().numpy().reshape(12, 1000), EPS)
+    assert_close(g.view.cpu().numpy().reshape(12, 1000), ref, torch.float32, "after injected")
