@@ -64,6 +64,25 @@ __device__ __forceinline__ Stat warp_merge(Stat s) {
   return s;
 }
 
+// warp_merge for partials of equal count in every lane of the segment (slices
+// that fill their threads' slots exactly): each step merges two partials of
+// the same count, so the weight b.n/n is exactly 1/2 and the count need not
+// travel. The arithmetic is chan_merge's with that weight (the same bits),
+// without its division and zero checks.
+template <int WIDTH>
+__device__ __forceinline__ Stat warp_merge_eq(Stat s) {
+#pragma unroll
+  for (int off = WIDTH / 2; off > 0; off >>= 1) {
+    const float om = __shfl_down_sync(kFullMask, s.mean, off, WIDTH);
+    const float o2 = __shfl_down_sync(kFullMask, s.m2, off, WIDTH);
+    const float d = om - s.mean;
+    s.mean = fmaf(d, 0.5f, s.mean);
+    s.m2 = s.m2 + o2 + d * d * (s.n * 0.5f);
+    s.n = s.n + s.n;
+  }
+  return s;
+}
+
 // ---------------------------------------------------------------------------
 // Element storage: a "slot" is one 16-byte vector of W = 16/sizeof(T)
 // elements, kept in registers as a uint4 in the input type's encoding.
@@ -106,6 +125,24 @@ struct Elem<__nv_bfloat16> {
     else
       asm volatile("shl.b32 %0, %1, 16;" : "=r"(r) : "r"(w));
     return __uint_as_float(r);
+  }
+  // (low / high value of the word w) - c in one instruction: the
+  // mixed-precision subtraction (sub.rn.f32.bf16, PTX ISA) takes the bf16
+  // operand from its half of the word; widening bf16 to fp32 is exact, so the
+  // result is the fp32 subtraction's, rounded once (the same bits as
+  // widening and subtracting). Used by the packed-pair forms, where it
+  // replaces a widening and a paired addition.
+  __device__ static __forceinline__ float diff_lo(unsigned w, float c) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tsub.rn.f32.bf16 %0, lo, %2;\n\t}"
+        : "=f"(r) : "r"(w), "f"(c));
+    return r;
+  }
+  __device__ static __forceinline__ float diff_hi(unsigned w, float c) {
+    float r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tsub.rn.f32.bf16 %0, hi, %2;\n\t}"
+        : "=f"(r) : "r"(w), "f"(c));
+    return r;
   }
   __device__ static __forceinline__ void set(uint4& v, int j, float f) {
     // f is a bf16 value widened to fp32 (exact), so its low 16 bits are zero

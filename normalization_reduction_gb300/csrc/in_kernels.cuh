@@ -105,44 +105,46 @@ __device__ __forceinline__ Stat tile_stat(const uint4 (&r)[NV], int nvalid) {
 }
 
 // Packed pair arithmetic for bf16 inputs: the two values of one 32-bit word of
-// a slot (elements 2i, 2i+1) widened into an fp32 pair and processed by one
-// f32x2 instruction (__fadd2_rn / __ffma2_rn), which halves the floating-point
-// instructions of slices that are issue-bound (a byte of bf16 holds twice the
-// values of fp32).
-__device__ __forceinline__ float2 bf16_pair_opaque(unsigned w) {
-  unsigned lo, hi;
-  asm volatile("shl.b32 %0, %1, 16;" : "=r"(lo) : "r"(w));
-  asm volatile("and.b32 %0, %1, 0xffff0000;" : "=r"(hi) : "r"(w));
-  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+// a slot (elements 2i, 2i+1) less a constant, as an fp32 pair, processed by
+// one f32x2 instruction (__fadd2_rn / __ffma2_rn), which halves the
+// floating-point instructions of slices that are issue-bound (a byte of bf16
+// holds twice the values of fp32). The pair comes from two mixed-precision
+// subtractions (Elem<bf16>::diff_lo / diff_hi): the same bits as widening the
+// pair and adding (-c, -c), one instruction fewer per pair (bf16 S = 2^20:
+// 5698 -> 5838 GB/s). The scalar loops keep the widening: there the mixed
+// form measured 2-4 % slower (S = 256, 4096, 16384, 65536).
+__device__ __forceinline__ float2 bf16_pair_diff(unsigned w, float c) {
+  using E = Elem<__nv_bfloat16>;
+  return make_float2(E::diff_lo(w, c), E::diff_hi(w, c));
 }
 
-// Shifted sums of a thread's bf16 values in one pass: d = x - K (nk = (-K, -K),
-// K the thread's first value), s += d, q += d^2, as pairs (words 0, 2 into 01;
+// Shifted sums of a thread's bf16 values in one pass: d = x - K (K the
+// thread's first value), s += d, q += d^2, as pairs (words 0, 2 into 01;
 // 1, 3 into 23). mean = K + S/n and M2 = Q - S^2/n follow; K is one of the
 // values, so (K - mean)^2 <= M2 and the cancellation is bounded by the
 // thread's count (at most 128 values in the kernels that use it).
-__device__ __forceinline__ void bf16_acc_onepass(const uint4& v, float2 nk, float2& s01, float2& s23,
+__device__ __forceinline__ void bf16_acc_onepass(const uint4& v, float K, float2& s01, float2& s23,
                                                  float2& q01, float2& q23) {
-  float2 d = __fadd2_rn(bf16_pair_opaque(v.x), nk);
+  float2 d = bf16_pair_diff(v.x, K);
   s01 = __fadd2_rn(s01, d);
   q01 = __ffma2_rn(d, d, q01);
-  d = __fadd2_rn(bf16_pair_opaque(v.y), nk);
+  d = bf16_pair_diff(v.y, K);
   s23 = __fadd2_rn(s23, d);
   q23 = __ffma2_rn(d, d, q23);
-  d = __fadd2_rn(bf16_pair_opaque(v.z), nk);
+  d = bf16_pair_diff(v.z, K);
   s01 = __fadd2_rn(s01, d);
   q01 = __ffma2_rn(d, d, q01);
-  d = __fadd2_rn(bf16_pair_opaque(v.w), nk);
+  d = bf16_pair_diff(v.w, K);
   s23 = __fadd2_rn(s23, d);
   q23 = __ffma2_rn(d, d, q23);
 }
 
 // o = (v - mean) * a + b
-__device__ __forceinline__ void bf16_norm(const uint4& v, float2 nm, float2 a2, float2 b2, float (&o)[8]) {
+__device__ __forceinline__ void bf16_norm(const uint4& v, float mean, float2 a2, float2 b2, float (&o)[8]) {
   const unsigned w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 r = __ffma2_rn(__fadd2_rn(bf16_pair_opaque(w[i]), nm), a2, b2);
+    const float2 r = __ffma2_rn(bf16_pair_diff(w[i], mean), a2, b2);
     o[2 * i] = r.x;
     o[2 * i + 1] = r.y;
   }
@@ -152,19 +154,22 @@ __device__ __forceinline__ int clamp_int(int64_t v, int lo, int hi) {
   return v < lo ? lo : (v > hi ? hi : static_cast<int>(v));
 }
 
-// Warp partials -> one CTA partial (valid in thread 0 of warp 0).
+// Warp partials -> one CTA partial (valid in thread 0 of warp 0). `uniform`
+// (the same for every thread of the CTA): every thread holds a partial of the
+// same count, so the merges take the equal-count form (warp_merge_eq: the
+// same tree and the same bits, no division).
 template <int THREADS>
-__device__ __forceinline__ Stat cta_merge(Stat st, Stat* warp_part) {
+__device__ __forceinline__ Stat cta_merge(Stat st, Stat* warp_part, bool uniform = false) {
   constexpr int NWARP = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  st = warp_merge<32>(st);
+  st = uniform ? warp_merge_eq<32>(st) : warp_merge<32>(st);
   if (NWARP == 1) return st;
   if (lane == 0) warp_part[warp] = st;
   __syncthreads();
   Stat s2 = stat_empty();
   if (warp == 0) {
     if (lane < NWARP) s2 = warp_part[lane];
-    s2 = warp_merge<32>(s2);
+    s2 = uniform ? warp_merge_eq<(NWARP > 1 ? NWARP : 2)>(s2) : warp_merge<32>(s2);
   }
   return s2;
 }
@@ -624,14 +629,13 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
     if (kPackedBf16 && nvalid > 0) {
       // one pass of shifted sums as pairs (bf16_acc_onepass)
       const float K = E::get_opaque(ns_valid > 0 ? stage[tid] : r[0], 0);
-      const float2 nk = make_float2(-K, -K);
       float2 s01 = make_float2(0.f, 0.f), s23 = s01, q01 = s01, q23 = s01;
 #pragma unroll
       for (int k = 0; k < NS; ++k)
-        if (k < ns_valid) bf16_acc_onepass(stage[k * THREADS + tid], nk, s01, s23, q01, q23);
+        if (k < ns_valid) bf16_acc_onepass(stage[k * THREADS + tid], K, s01, s23, q01, q23);
 #pragma unroll
       for (int k = 0; k < NR; ++k)
-        if (k < nr_valid) bf16_acc_onepass(r[k], nk, s01, s23, q01, q23);
+        if (k < nr_valid) bf16_acc_onepass(r[k], K, s01, s23, q01, q23);
       const float n = static_cast<float>(nvalid);
       const float sd = (s01.x + s01.y) + (s23.x + s23.y), qd = (q01.x + q01.y) + (q23.x + q23.y);
       st = Stat{n, K + sd / n, fmaxf(qd - sd * (sd / n), 0.f)};
@@ -679,7 +683,13 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
       }
       st = Stat{n, mean, (q4[0] + q4[1]) + (q4[2] + q4[3])};
     }
-    const Stat cta = cta_merge<THREADS>(st, warp_part);
+    // equal-count merges where every thread of the CTA holds its full share,
+    // in the packed form only: there the merge lies between the data's
+    // arrival and the cluster exchange (bf16 S = 2^20: 5838 -> 6240 GB/s);
+    // in the scalar kernels it measured 3-7 % slower (fewer instructions,
+    // but the loads' latency more exposed: long-scoreboard stalls 3.6 -> 5.4
+    // per issue at S = 16384)
+    const Stat cta = cta_merge<THREADS>(st, warp_part, kPackedBf16 && cvec == kChunk);
     const float2 mr = cluster_exchange<THREADS>(cta, slots, xbar, &fin, csize, crank, it, p.eps,
                                                 p.err, xfailed);
     if (crank == 0 && tid == 0) {
@@ -695,7 +705,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
         const uint4 v = stage[k * THREADS + tid];
         float o[W];
         if constexpr (kPackedBf16) {
-          bf16_norm(v, make_float2(-mr.x, -mr.x), make_float2(ab.x, ab.x), make_float2(ab.y, ab.y), o);
+          bf16_norm(v, mr.x, make_float2(ab.x, ab.x), make_float2(ab.y, ab.y), o);
         } else {
 #pragma unroll
           for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(v, j) - mr.x, ab.x, ab.y);
@@ -717,7 +727,7 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
       if (k < nr_valid) {
         float o[W];
         if constexpr (kPackedBf16) {
-          bf16_norm(r[k], make_float2(-mr.x, -mr.x), make_float2(ab.x, ab.x), make_float2(ab.y, ab.y), o);
+          bf16_norm(r[k], mr.x, make_float2(ab.x, ab.x), make_float2(ab.y, ab.y), o);
         } else {
 #pragma unroll
           for (int j = 0; j < W; ++j) o[j] = fmaf(E::get_opaque(r[k], j) - mr.x, ab.x, ab.y);
