@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(THREADS, 4) bn_stats_kernel(const BnParams p) 
 // its staged values, and merges the two.
 template <int THREADS, int NR, int NS>
 __global__ void __launch_bounds__(THREADS, 4) bn_stats_split_kernel(const BnParams p) {
-  extern __shared__ __align__(16) uint4 stage[];   // (THREADS * NS) vectors
+  extern __shared__ __align__(128) uint4 stage[];   // (THREADS * NS) vectors
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ uint64_t bar;
   __shared__ uint64_t dbg_bar;
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 4) bn_apply_kernel(const BnParams p) 
 // statistics merge and side outputs as bn_apply_kernel.
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnParams p) {
-  extern __shared__ __align__(16) uint4 stage[];   // kBnChunk / 4 vectors
+  extern __shared__ __align__(128) uint4 stage[];   // kBnChunk / 4 vectors
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ float4 coef;
   __shared__ uint64_t bar;
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
 // ---------------------------------------------------------------------------
 template <int THREADS, int NR, int NS>
 __global__ void __launch_bounds__(THREADS, 4) bn_resident_kernel(const BnParams p) {
-  extern __shared__ __align__(16) uint4 stage[];   // THREADS * NS vectors
+  extern __shared__ __align__(128) uint4 stage[];   // THREADS * NS vectors
   __shared__ Stat warp_part[THREADS / 32];
   __shared__ float4 coef;
   __shared__ uint64_t bar;
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(THREADS) bn_eval_kernel(const BnParams p) {
 // while the channel's coefficients are formed.
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 3) bn_eval_staged_kernel(const BnParams p) {
-  extern __shared__ __align__(16) uint4 stage[];   // kBnChunk / 4 vectors
+  extern __shared__ __align__(128) uint4 stage[];   // kBnChunk / 4 vectors
   __shared__ uint64_t bar;
   __shared__ uint64_t dbg_bar;
   const int tid = threadIdx.x;

@@ -42,9 +42,9 @@ namespace fnorm {
 // exchanged, coefficients formed, kept part written, sample done -- into
 // g_epi_phase[cta][phase], read by fnorm_phase_trace_read (each launch
 // overwrites the previous one's stamps).
+#ifdef FNORM_PHASE_TRACE
 constexpr int kEpiPhases = 6;
 constexpr int kEpiPhaseCtas = 2048;
-#ifdef FNORM_PHASE_TRACE
 __device__ unsigned long long g_epi_phase[kEpiPhaseCtas * kEpiPhases];
 #define FNORM_EPI_STAMP(k)                                                      \
   if (tid == 0 && it == 0 && blockIdx.x < kEpiPhaseCtas)                      \
