@@ -103,6 +103,17 @@ __device__ __forceinline__ float epi_zc(float v, const float4& k) {
 // thread). For the page's shape a sample is 806 KB and the whole input
 // 103 MB, below the 126 MB L2; with 256-thread CTAs in 4-CTA clusters every
 // sample's cluster is resident at once, so HBM still sees one read of x.
+// 16-byte load cached in L2 only (ld.global.cg): the statistics pass's reads
+// of x. Measured on the page's shape: 28.7 against 29.0 us per call with the
+// read-only path (__ldg); the output pass keeps its streaming loads (.cg there
+// was slower: 31.6 us), and loads that skip the L1 allocation were slower in
+// either pass (34.4 us).
+__device__ __forceinline__ uint4 ld_v4_l2(const void* p) {
+  uint4 v;
+  asm("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 template <bool WANT_ARG>
 __device__ __forceinline__ void epi_take(const uint4& u, const float4& k, int c, float (&best)[4],
                                          int (&arg)[4]) {
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       for (; t + 32 * U <= vr; t += 32 * U) {   // full tiles
         uint4 r[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) r[u] = ld_v4(xc + t + u * 32);
+        for (int u = 0; u < U; ++u) r[u] = ld_v4_l2(xc + t + u * 32);
         if (t == 0) {
 #pragma unroll
           for (int u = 0; u < U; ++u)
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const bool v = t + u * 32 + lane < vr;
-          r[u] = v ? ld_v4(xc + t + u * 32) : make_uint4(0, 0, 0, 0);
+          r[u] = v ? ld_v4_l2(xc + t + u * 32) : make_uint4(0, 0, 0, 0);
           nvalid += v ? 4 : 0;
           if (t == 0 && v && u * 32 + lane < KS) keep[c * KS + u * 32 + lane] = r[u];
         }
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(THREADS, 4) epi_range_l2_kernel(const EpiParam
       for (; t < vr; t += 32) {                  // short tail: one vector per lane
         const bool v = t + lane < vr;
         uint4 r1[1];
-        r1[0] = v ? ld_v4(xc + t) : make_uint4(0, 0, 0, 0);
+        r1[0] = v ? ld_v4_l2(xc + t) : make_uint4(0, 0, 0, 0);
         if (v && t + lane < KS) keep[c * KS + t + lane] = r1[0];
         if (ONEPASS) {
           if (v) {
