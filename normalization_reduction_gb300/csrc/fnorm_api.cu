@@ -356,13 +356,16 @@ fnorm_status in_make_plan(int tin, int tout, const void* x, const void* y, int64
       plan.nv = std::atoi(u) == kStreamUnrollFew ? kStreamUnrollFew : kStreamUnroll;
   }
 
-  // bf16 slices spread over clusters of more than 8 CTAs take the packed pair
-  // arithmetic (shapes with 8 register and 8 staged slots); FNORM_NO_PACK=1
-  // keeps the scalar loops
+  // bf16 slices spread over clusters of more than 8 CTAs (shapes with 8
+  // register and 8 staged slots) and slices held by one 64-thread CTA (8
+  // register slots) take the packed pair arithmetic; FNORM_NO_PACK=1 keeps the
+  // scalar loops
   auto set_packed = [&] {
-    plan.packed = plan.path == InPath::kSplit && tin == 1 && plan.cluster > 8 && plan.nv == 8 &&
-                  plan.ns == 8 && (plan.threads == 256 || plan.threads == 512 ||
-                                   plan.threads == 1024) && !env("FNORM_NO_PACK");
+    const bool clustered = plan.cluster > 8 && plan.ns == 8 &&
+                           (plan.threads == 256 || plan.threads == 512 || plan.threads == 1024);
+    const bool small = plan.cluster == 1 && plan.ns == 0 && plan.threads == 64;
+    plan.packed = plan.path == InPath::kSplit && tin == 1 && plan.nv == 8 && (clustered || small) &&
+                  !env("FNORM_NO_PACK");
   };
   set_packed();
   int cap = in_capacity(tin, tout, plan);

@@ -563,9 +563,11 @@ __global__ void __launch_bounds__(THREADS, split_min_blocks(THREADS, NR))
   // normalisation, both as packed pairs (bf16_acc_onepass, bf16_norm). The
   // plan sets PACK for slices spread over clusters of more than 8 CTAs, where
   // a slice's arithmetic sits between the arrival of its data and the cluster
-  // exchange (bf16 S = 2^20, 16-CTA clusters: 5002 -> 5720 GB/s); with 8 or 1
-  // CTAs per slice the same code measured 0.5-4 % slower, and those keep the
-  // exact two-pass scalar loops.
+  // exchange (bf16 S = 2^20, 16-CTA clusters: 5002 -> 5720 GB/s, 6235 with the
+  // mixed-precision pairs and equal-count merges), and for slices held by one
+  // 64-thread CTA (bf16 S = 4096: 5967-5995 -> 6130-6143 GB/s); with 8, 4 or
+  // 1 larger CTAs per slice it measured 2-7 % slower (S = 16384 ... 2^18), and
+  // those keep the exact two-pass scalar loops.
   constexpr bool kPackedBf16 = PACK && W == 8;
   extern __shared__ __align__(128) uint4 stage[];   // [NS][THREADS] slots
   __shared__ Stat warp_part[THREADS / 32];
@@ -854,6 +856,7 @@ static void* pick_kernel(const InPlan& plan) {
   if (plan.threads == T && plan.nv == R && plan.ns == SM)            \
     return reinterpret_cast<void*>(&in_split_kernel<Tin, Tout, T, R, SM, true>);
           FNORM_SPLIT_P(256, 8, 8) FNORM_SPLIT_P(512, 8, 8) FNORM_SPLIT_P(1024, 8, 8)
+          FNORM_SPLIT_P(64, 8, 0)
 #undef FNORM_SPLIT_P
         }
         return nullptr;

@@ -253,7 +253,8 @@ def test_few_long_slices(orc, shape, dt):
 
 
 PACKED_CASES = [(3, 1 << 20, None), (2, 1047776, None), (3, 300000, "split:256:8:8:12"),
-                (2, 600000, "split:512:8:8:10"), (4, 262144, None)]
+                (2, 600000, "split:512:8:8:10"), (4, 262144, None),
+                (300, 4096, None), (37, 3000, None), (5, 2056, None)]
 
 
 @pytest.mark.parametrize("NC,S,path", PACKED_CASES,
@@ -261,12 +262,14 @@ PACKED_CASES = [(3, 1 << 20, None), (2, 1047776, None), (3, 300000, "split:256:8
 @pytest.mark.parametrize("tout", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 @pytest.mark.parametrize("dist", ["normal", "shifted"])
 def test_bf16_packed_matches_scalar(orc, fnorm_env, NC, S, path, tout, dist):
-    """bf16 slices spread over clusters of more than 8 CTAs take one pass of
-    shifted sums and packed pair arithmetic (two fp32 lanes per instruction);
+    """bf16 slices spread over clusters of more than 8 CTAs, and slices of
+    2049-4096 values held by one 64-thread CTA, take one pass of shifted sums
+    and packed pair arithmetic (two fp32 lanes per instruction);
     FNORM_NO_PACK=1 gives the exact two-pass scalar loops. Both must match the
     oracle (outputs, means, rstd) and each other within the tolerance. The
-    last case (8-CTA clusters) runs the scalar loops both times and must be
-    bit-identical."""
+    case S = 262144 (8-CTA clusters) runs the scalar loops both times and must
+    be bit-identical. S = 4096 fills every thread's slots (equal-count merges);
+    3000 and 2056 leave threads partly or wholly empty."""
     if path:
         fnorm_env.setenv("FNORM_FORCE_PATH", path)
     x = make_x(NC, S, torch.bfloat16, 5150 + S % 997, dist)
@@ -282,10 +285,12 @@ def test_bf16_packed_matches_scalar(orc, fnorm_env, NC, S, path, tout, dist):
         assert torch.equal(y1, y2) and torch.equal(m1, m2) and torch.equal(r1, r2)
 
 
-@pytest.mark.parametrize("S,threads,chunk", [(1 << 20, 512, 8192), (1 << 19, 256, 4096)])
+@pytest.mark.parametrize("S,threads,chunk", [(1 << 20, 512, 8192), (1 << 19, 256, 4096),
+                                             (4096, 64, 512)])
 def test_bf16_packed_outliers_at_thread_shifts(orc, S, threads, chunk):
     """The packed form's one-pass sums are shifted by each thread's first value
-    (its first staged vector: vector r*chunk + t of CTA r's chunk, element 0).
+    (its first staged vector, or its first register vector when the CTA stages
+    nothing: vector r*chunk + t of CTA r's chunk, element 0).
     An outlier there is their worst case: put one at every thread's shift, on
     data with a large offset, and compare with the oracle (fp32 output)."""
     NC = 2
