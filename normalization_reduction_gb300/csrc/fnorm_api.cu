@@ -443,7 +443,8 @@ fnorm_status epi_make_plan(const float* x, const float* y, const int64_t* argmax
     const int64_t nv4 = S / 4;
     const int64_t per = (nv4 + cl - 1) / cl;
     const int cl_eff = static_cast<int>((nv4 + per - 1) / per);
-    int keep = static_cast<int>(kEpiKeepBudget / (C * 16));
+    const int64_t fixed = static_cast<int64_t>(epi_range_l2_smem(C, cl_eff, 0));
+    int keep = fixed < kEpiSmemBudget ? static_cast<int>((kEpiSmemBudget - fixed) / (C * 16)) : 0;
     if (keep > kEpiKeepMax) keep = kEpiKeepMax;
     if (keep > per) keep = static_cast<int>(per);
     if (const char* k = env("FNORM_EPI_KEEP")) keep = std::atoi(k) < keep ? std::atoi(k) : keep;

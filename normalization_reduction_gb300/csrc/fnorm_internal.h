@@ -111,12 +111,20 @@ cudaError_t epi_launch(const EpiParams& p, const EpiPlan& plan, cudaStream_t str
 int epi_max_active_clusters(const EpiPlan& plan);
 size_t epi_range_l2_smem(int64_t C, int cluster, int keep);
 // L2 path: the leading position vectors of each channel of a CTA's range that
-// stay in shared memory from the statistics pass to the output pass.
-constexpr int kEpiKeepMax = 160;
+// stay in shared memory from the statistics pass to the output pass: as many
+// as fit kEpiSmemBudget (118 for 16 channels in 4-CTA clusters), at most
+// kEpiKeepMax (compiled in for that case).
+constexpr int kEpiKeepMax = 118;
 // L2 path: CTA ranges of at most this many position vectors (at most 40 per
 // lane, 160 values) take the shifted one-pass lane sums for the statistics.
 constexpr int64_t kEpiOnePassMaxPer = 1280;
-constexpr int kEpiKeepBudget = 40960;   // bytes (keeps the CTA under 48 KB of dynamic smem)
+// L2 path: dynamic shared memory per CTA, kept part included, such that four
+// CTAs per SM (with their static shared memory and the 1 KB per CTA the
+// system reserves) fit the 132 KB shared-memory carveout; the rest of the
+// SM's 256 KB stays L1, which this kernel's loads need in flight (page's
+// shape: 28.7 us per call keeping 160 vectors per channel with a 196 KB
+// carveout, 28.1 us keeping 118; 96 or 64 kept, same carveout: 28.8 us).
+constexpr int kEpiSmemBudget = 33 * 1024 - 1024 - 64;
 size_t epi_stream_smem(int64_t C, int cluster);
 
 // ---------------------------------------------------------------- BatchNorm
