@@ -228,3 +228,26 @@ def test_outliers_at_lane_shifts(orc, fnorm_env, S, want_arg, form):
         check(orc, x, m, what=f"lane-shift outliers S={S} {form}")
     else:
         check_no_arg(orc, x, m, what=f"lane-shift outliers S={S} {form} no index")
+
+
+def _epi_plan(capfd):
+    err = capfd.readouterr().err
+    lines = [ln for ln in err.splitlines() if "fnorm_instancenorm_epilogue plan" in ln]
+    assert lines, err[-2000:]
+    return dict(kv.split("=") for kv in lines[-1].split(": ", 1)[1].split())
+
+
+@pytest.mark.parametrize("C,keep", [(16, 118), (32, 54), (1, 118)])
+def test_kept_part_fits_the_carveout_budget(orc, fnorm_env, capfd, C, keep):
+    """The L2-form plan keeps as many leading vectors per channel in shared
+    memory as fit 33 KB per CTA with its other shared memory (four CTAs per SM
+    in the 132 KB shared-memory carveout, the rest of the SM left to L1), at
+    most 118: 118 for the page's 16 channels, 54 for 32. The outputs still
+    match the oracle."""
+    fnorm_env.setenv("FNORM_DEBUG_PLAN", "1")
+    x, m = inputs.epilogue(dev(), shape=(3, C, 14, 30, 30))
+    check(orc, x, m, what=f"C={C}")
+    plan = _epi_plan(capfd)
+    assert plan["path"] == "2" and int(plan["cluster"]) == 4
+    assert int(plan["keep"]) == keep
+    assert int(plan["smem"]) <= 33 * 1024 - 1024 - 64
