@@ -104,10 +104,11 @@ __device__ __forceinline__ float epi_zc(float v, const float4& k) {
 // 103 MB, below the 126 MB L2; with 256-thread CTAs in 4-CTA clusters every
 // sample's cluster is resident at once, so HBM still sees one read of x.
 // 16-byte load cached in L2 only (ld.global.cg): the statistics pass's reads
-// of x. Measured on the page's shape: 28.7 against 29.0 us per call with the
-// read-only path (__ldg); the output pass keeps its streaming loads (.cg there
-// was slower: 31.6 us), and loads that skip the L1 allocation were slower in
-// either pass (34.4 us).
+// of x. Measured on the page's shape with 160 vectors kept per channel (60 KB
+// of L1): 28.7 against 29.0 us per call with the read-only path (__ldg); with
+// the current 118 (124 KB of L1) the two measure the same. The output pass
+// keeps its streaming loads (.cg there was slower: 31.6 us), and loads that
+// skip the L1 allocation were slower in either pass (34.4 us).
 __device__ __forceinline__ uint4 ld_v4_l2(const void* p) {
   uint4 v;
   asm("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
