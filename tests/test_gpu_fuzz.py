@@ -60,6 +60,28 @@ def test_fuzz_instancenorm(orc, case):
                  f"case {case}: N={N} C={C} S={S} {tin}->{tout} misalign={misalign}")
 
 
+@pytest.mark.parametrize("case", range(20))
+def test_fuzz_bf16_one_cta_slices(orc, case):
+    """bf16 slices of 2049-4096 values: one 64-thread CTA per slice, statistics
+    in one pass of shifted sums and packed pairs; slice lengths that fill the
+    threads' slots or leave some empty, both output types, offset and spread
+    drawn per case."""
+    rng = np.random.default_rng(9700 + case)
+    S = int(rng.integers(2049, 4097))
+    if rng.random() < 0.6:
+        S -= S % 8
+    C, N = int(rng.integers(1, 9)), int(rng.integers(1, 40))
+    tout = torch.bfloat16 if rng.random() < 0.5 else torch.float32
+    x = inputs.normal((N * C * S,), 9800 + case, dev(), mean=float(rng.uniform(-5, 5)),
+                      std=float(rng.uniform(0.05, 4.0))).to(torch.bfloat16)
+    g = Guarded((N * C * S,), tout)
+    fn.fnorm_instancenorm(x, g.view, N, C, S, code(torch.bfloat16), code(tout), EPS, None, None)
+    torch.cuda.synchronize()
+    g.check()
+    ref, _, _ = orc.instancenorm_affine(to_f64(x).reshape(N, C, S), None, None, EPS)
+    assert_close(to_f64(g.view).reshape(N, C, S), ref, tout, f"case {case}: N={N} C={C} S={S}")
+
+
 @pytest.mark.parametrize("case", range(CASES))
 def test_fuzz_epilogue(orc, case):
     rng = np.random.default_rng(9300 + case)
