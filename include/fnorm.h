@@ -86,7 +86,13 @@ typedef enum fnorm_dtype {
  * Every (in_dtype, out_dtype) pair of F32/BF16 is supported.
  * A slice is read from HBM once and written once whenever it fits in one
  * thread-block cluster (up to 2 MiB of input per slice); longer slices are
- * read twice (statistics pass, then normalisation pass).
+ * read twice (statistics pass, then normalisation pass). Out of place, with
+ * fp32 input and output, 16-byte aligned x and y, S a multiple of 4, S above
+ * 2^19 and N*C at most a quarter of the SM count, the few long slices are
+ * spread over all SMs as fnorm_instancenorm_ws does, with y itself holding
+ * the per-chunk statistics between the three launches (y's contents before
+ * the call completes are unspecified, as for any output); in place, or
+ * otherwise, each long slice is streamed by one cluster.
  * Statistics are accumulated in fp32 and merged in a fixed order: results are
  * deterministic for a given call shape and agree with the exact definition to
  * fp32 accuracy.
@@ -98,8 +104,10 @@ FNORM_API fnorm_status fnorm_instancenorm(const void* x, void* y, int64_t N, int
 /*
  * fnorm_instancenorm with a caller workspace, for a few slices too long for
  * one thread-block cluster (more than 2 MiB of fp32 each, e.g. x[1,1,8192,8192]):
- * without one, each such slice is streamed by a single cluster and most SMs
- * stay idle. Same arguments, results and errors as fnorm_instancenorm, plus:
+ * the per-chunk statistics go to the workspace instead of y, which also serves
+ * in-place calls (fnorm_instancenorm streams those through one cluster per
+ * slice, leaving most SMs idle). Same arguments, results and errors as
+ * fnorm_instancenorm, plus:
  *
  *   workspace        device memory of at least
  *                    fnorm_instancenorm_workspace_size(N, C, S) bytes,

@@ -83,6 +83,8 @@ __device__ __forceinline__ BnUnit bn_unit(const BnParams& p, int64_t m) {
   return u;
 }
 __device__ __forceinline__ float4* bn_partial(const BnParams& p, const BnUnit& u) {
+  if (p.part_cstride)   // strided placement (InstanceNorm, output buffer as scratch)
+    return p.partials + u.c * p.part_cstride + (u.n * p.chunks + u.k) * p.part_kstride;
   return p.partials + u.c * (p.N * p.chunks) + u.n * p.chunks + u.k;
 }
 
@@ -222,7 +224,8 @@ __global__ void __launch_bounds__(THREADS, 4) bn_apply_kernel(const BnParams p) 
 
   // channel statistics: the channel's partials (or the ranks' statistics)
   // merged in a fixed order
-  const float4 cf = bn_channel_coef<THREADS, false>(p, c, p.stats + c * p.stats_cstride,
+  const float4 cf = bn_channel_coef<THREADS, false>(p, c, p.stats + c * p.stats_cstride +
+                                                             b * p.stats_kstride,
                                                     p.stats_count, p.stats_istride, b == 0,
                                                     warp_part, &coef);
 
@@ -285,9 +288,12 @@ __global__ void __launch_bounds__(THREADS, 3) bn_apply_staged_kernel(const BnPar
     mbar_arrive_expect_tx(&bar, static_cast<unsigned>(nvec) * 16u);
     tma_bulk_g2s(stage, p.x + off, static_cast<unsigned>(nvec) * 16u, &bar);
   }
-  const float4 cf = bn_channel_coef<THREADS, false>(p, u.c, p.stats + u.c * p.stats_cstride,
-                                                    p.stats_count, p.stats_istride,
-                                                    u.n == 0 && u.k == 0, warp_part, &coef);
+  // (with the output buffer as scratch, the unit's own copy of the
+  // statistics lies at the start of its output range: read here, before the
+  // barrier in bn_channel_coef, and overwritten by this CTA's stores below)
+  const float4 cf = bn_channel_coef<THREADS, false>(
+      p, u.c, p.stats + u.c * p.stats_cstride + (u.n * p.chunks + u.k) * p.stats_kstride,
+      p.stats_count, p.stats_istride, u.n == 0 && u.k == 0, warp_part, &coef);
   if (nvec > 0) {
     // a wait that gives up has flagged the error; it is retried once (bounded)
     // so that the copy is not in flight when the CTA leaves
@@ -573,7 +579,18 @@ __global__ void __launch_bounds__(THREADS) bn_merge_kernel(const BnParams p) {
     acc = chan_merge(acc, Stat{v.x, v.y, v.z});
   }
   const Stat s = cta_merge<THREADS>(acc, warp_part);
-  if (threadIdx.x == 0) p.local_out[c] = make_float4(s.n, s.mean, s.m2, 0.f);
+  if (p.local_copies > 1) {
+    // one copy per unit of the channel (output buffer as scratch): every
+    // thread has read its partials before cta_merge's barrier, and the copies
+    // overwrite them only after this one
+    __shared__ float4 merged;
+    if (threadIdx.x == 0) merged = make_float4(s.n, s.mean, s.m2, 0.f);
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < p.local_copies; i += THREADS)
+      p.local_out[c * p.local_cstride + i * p.local_kstride] = merged;
+  } else if (threadIdx.x == 0) {
+    p.local_out[c] = make_float4(s.n, s.mean, s.m2, 0.f);
+  }
   pdl_trigger();
 }
 

@@ -685,6 +685,48 @@ fnorm_status in_call(const char* name, const void* x, void* y, const float* gamm
     }
   }
 
+  // The same route without a workspace, for out-of-place calls: the output
+  // buffer holds the per-unit statistics between the launches. Unit (q, k)
+  // (slice q, 64 KiB chunk k) writes its partial into the first 16 bytes of
+  // its own output range; one CTA per slice merges the slice's partials and
+  // writes the result back into every one of those slots; the apply CTA of
+  // each unit reads its own slot before it overwrites its range with outputs.
+  // No CTA writes bytes another CTA still has to read.
+  if (!workspace && tin == 0 && tout == 0 && !gamma && !beta && x != y && in_ws_shape(NC, S) &&
+      aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_PATH") &&
+      !env("FNORM_FORCE_SCALAR")) {
+    unsigned* err = err_word();
+    if (!err) return FNORM_ERR_CUDA;
+    BnParams p{};
+    bn_fill(&p, static_cast<const float*>(x), static_cast<float*>(y), nullptr, nullptr, 1.f,
+            nullptr, nullptr, 0.f, eps, mean_out, rstd_out, 1, NC, S, err);
+    if (p.vec && p.split) {
+      if (env("FNORM_DEBUG_PLAN"))
+        std::fprintf(stderr, "fnorm_instancenorm plan: route=output_scratch NC=%lld S=%lld units=%lld\n",
+                     static_cast<long long>(NC), static_cast<long long>(S),
+                     static_cast<long long>(p.chunks));
+      float4* slots = static_cast<float4*>(y);
+      const int64_t slice4 = S / 4, unit4 = p.chunk / 4;
+      p.partials = slots;
+      p.part_cstride = slice4;
+      p.part_kstride = unit4;
+      p.stats = slots;
+      p.stats_cstride = slice4;
+      p.stats_istride = unit4;
+      p.stats_count = p.chunks;
+      p.local_out = slots;
+      p.local_cstride = slice4;
+      p.local_kstride = unit4;
+      p.local_copies = p.chunks;
+      cudaError_t e = bn_launch_local_stats(p, cs);
+      if (e != cudaSuccess) return cuda_status(e);
+      p.stats_istride = 0;
+      p.stats_count = 1;
+      p.stats_kstride = unit4;
+      return cuda_status(bn_launch_apply(p, cs));
+    }
+  }
+
   InPlan plan;
   fnorm_status st = in_make_plan(tin, tout, x, y, NC, S, &plan);
   if (st != FNORM_OK) return st;

@@ -154,6 +154,19 @@ struct BnParams {
   int64_t stats_istride;
   int64_t stats_count;
   float4* local_out;    // [C] merged local statistics (local-stats call), else null
+  // Strided placement, for InstanceNorm on few long slices with the output
+  // buffer as scratch (zero: the workspace layouts above). The partial of unit
+  // (c, n, k) goes to partials[c * part_cstride + (n * chunks + k) * part_kstride];
+  // the merge writes local_copies copies of channel c's statistics to
+  // local_out[c * local_cstride + i * local_kstride]; the apply pass reads
+  // unit (c, n, k)'s statistics from stats + c * stats_cstride + (n * chunks +
+  // k) * stats_kstride.
+  int64_t part_cstride;
+  int64_t part_kstride;
+  int64_t local_cstride;
+  int64_t local_kstride;
+  int64_t local_copies;
+  int64_t stats_kstride;
   unsigned* grid_counter;  // resident kernel: grid-barrier arrivals (zeroed before the launch)
   bool vec;
   bool split;           // statistics pass by the register + TMA-staged kernel (vector mode)

@@ -124,3 +124,17 @@ def test_graph_instancenorm_workspace_route():
             fn.fnorm_instancenorm_ws(x, y, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None,
                                      ws, nb, torch.cuda.current_stream())
     _capture_and_compare(run, ys)
+
+
+def test_graph_instancenorm_output_scratch_route():
+    """fnorm_instancenorm without a workspace on few long fp32 slices (three
+    launches that keep the per-unit statistics in the output buffer) under
+    graph capture: replays equal an eager call."""
+    N, C, S = 1, 2, 1 << 20
+    x = inputs.normal((N, C, S), 23, dev())
+    y = torch.empty_like(x)
+
+    def run():
+        fn.fnorm_instancenorm(x, y, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None,
+                              torch.cuda.current_stream())
+    _capture_and_compare(run, [y])

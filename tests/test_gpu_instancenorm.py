@@ -351,6 +351,49 @@ def test_workspace_entry_point(orc, shape, dtype):
         assert e.value.status == fn.Status.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 4096, 4100), (1, 3, 2048, 2048), (8, 3, 1024, 1024),
+                                   (38, 1, 1024, 1024), (2, 1, 1000, 1004)])
+def test_long_slices_without_workspace(orc, fnorm_env, capfd, shape):
+    """fnorm_instancenorm (no workspace) on few fp32 slices longer than a
+    cluster holds, out of place: the output buffer carries the per-unit
+    statistics between its launches. Element-wise against the oracle with the
+    mean and rstd outputs and guard bands around y; y starts dirty. The plan
+    line shows the route; with more than 1024 units per slice the result is
+    the workspace route's bit for bit (same kernels, same merge order). An
+    in-place call on the same shape takes the cluster stream and still
+    matches."""
+    N, C = shape[0], shape[1]
+    S = int(np.prod(shape[2:]))
+    fnorm_env.setenv("FNORM_DEBUG_PLAN", "1")
+    x = inputs.normal((N, C, S), 1401 + C, dev(), mean=-2.5, std=3.0)
+    g = Guarded((N, C, S), torch.float32)
+    g.view.fill_(float("nan"))
+    mean = torch.empty(N * C, device=dev())
+    rstd = torch.empty(N * C, device=dev())
+    fn.fnorm_instancenorm(x, g.view, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, mean, rstd)
+    torch.cuda.synchronize()
+    g.check()
+    assert fn.fnorm_get_last_error() == fn.Status.OK
+    assert "route=output_scratch" in capfd.readouterr().err
+    ref, rmean, rvar = orc.instancenorm(x.cpu().numpy().reshape(N * C, S), EPS)
+    assert_close(g.view.cpu().numpy().reshape(N * C, S), ref, torch.float32, f"no ws {shape}")
+    assert np.max(np.abs(mean.cpu().numpy() - rmean)) <= 1e-5
+    assert np.allclose(rstd.cpu().numpy(), 1 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)
+    if S // 16384 >= 1024:
+        nb = fn.fnorm_instancenorm_workspace_size(N, C, S)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev())
+        y2 = torch.empty_like(x)
+        fn.fnorm_instancenorm_ws(x, y2, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None,
+                                 ws, nb)
+        torch.cuda.synchronize()
+        assert torch.equal(y2, g.view)
+    xi = x.clone()
+    fn.fnorm_instancenorm(xi, xi, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS, None, None)
+    torch.cuda.synchronize()
+    assert "route=output_scratch" not in capfd.readouterr().err
+    assert_close(xi.cpu().numpy().reshape(N * C, S), ref, torch.float32, f"in place {shape}")
+
+
 def test_injected_launch_failure_leaves_outputs_untouched(orc):
     """A call failed by fnorm_debug_fail_launches raises FNORM_ERR_CUDA and
     writes nothing; the next call runs normally."""
