@@ -270,12 +270,16 @@ def instance_norm(x, eps: float = 1e-5, out_dtype=None, out=None, return_stats: 
     if return_stats:
         mean = torch.empty(N * C, dtype=torch.float32, device=x.device)
         rstd = torch.empty(N * C, dtype=torch.float32, device=x.device)
-    if weight is None and bias is None:
-        # few slices too long for one cluster take the workspace route
+    if weight is None and bias is None and y.data_ptr() == x.data_ptr():
+        # in place, few slices too long for one cluster need a workspace to
+        # use every SM (out of place the library keeps their statistics in y)
         nb = fnorm_instancenorm_workspace_size(N, C, S)
         ws = torch.empty(nb, dtype=torch.uint8, device=x.device) if nb else None
         fnorm_instancenorm_ws(x, y, N, C, S, _dtype_code(x.dtype), _dtype_code(y.dtype), eps,
                               mean, rstd, ws, nb, stream)
+    elif weight is None and bias is None:
+        fnorm_instancenorm(x, y, N, C, S, _dtype_code(x.dtype), _dtype_code(y.dtype), eps, mean,
+                           rstd, stream)
     else:
         fnorm_instancenorm_affine(x, y, weight, bias, N, C, S, _dtype_code(x.dtype),
                                   _dtype_code(y.dtype), eps, mean, rstd, stream)

@@ -414,3 +414,22 @@ def test_injected_launch_failure_leaves_outputs_untouched(orc):
     g.check()
     ref, _, _ = orc.instancenorm(x.cpu().numpy().reshape(12, 1000), EPS)
     assert_close(g.view.cpu().numpy().reshape(12, 1000), ref, torch.float32, "after injected")
+
+
+@pytest.mark.parametrize("in_place", [False, True], ids=["out_of_place", "in_place"])
+def test_torch_helper_long_slices(orc, in_place):
+    """The torch helper instance_norm on few long fp32 slices: out of place it
+    calls fnorm_instancenorm (statistics kept in y), in place
+    fnorm_instancenorm_ws with a workspace it allocates; both match the
+    oracle, with the statistics outputs."""
+    N, C, S = 1, 2, 1 << 20
+    x = inputs.normal((N, C, 1024, 1024), 1601, dev(), mean=0.5, std=1.5)
+    ref, rmean, rvar = orc.instancenorm(x.cpu().numpy().reshape(N * C, S), EPS)
+    xin = x.clone() if in_place else x
+    y, mean, rstd = fn.instance_norm(xin, out=xin if in_place else None, return_stats=True)
+    torch.cuda.synchronize()
+    if in_place:
+        assert y.data_ptr() == xin.data_ptr()
+    assert_close(y.cpu().numpy().reshape(N * C, S), ref, torch.float32, "helper")
+    assert np.max(np.abs(mean.cpu().numpy() - rmean)) <= 1e-5
+    assert np.allclose(rstd.cpu().numpy(), 1 / np.sqrt(rvar + EPS), rtol=2e-6, atol=0)
