@@ -91,8 +91,9 @@ typedef enum fnorm_dtype {
  * 2^19 and N*C at most a quarter of the SM count, the few long slices are
  * spread over all SMs as fnorm_instancenorm_ws does, with y itself holding
  * the per-chunk statistics between the three launches (y's contents before
- * the call completes are unspecified, as for any output); in place, or
- * otherwise, each long slice is streamed by one cluster.
+ * the call completes are unspecified, as for any output); the same holds for
+ * fnorm_instancenorm_affine. In place, or otherwise, each long slice is
+ * streamed by one cluster.
  * Statistics are accumulated in fp32 and merged in a fixed order: results are
  * deterministic for a given call shape and agree with the exact definition to
  * fp32 accuracy.

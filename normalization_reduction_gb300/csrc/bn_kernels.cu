@@ -174,8 +174,9 @@ __device__ __forceinline__ float4 bn_channel_coef(const BnParams& p, int64_t c, 
   if (threadIdx.x == 0) {
     const float var = s.m2 / s.n;
     const float rstd = rsqrtf(var + p.eps);
-    const float g = p.gamma ? p.gamma[c] : 1.f;
-    const float bt = p.beta ? p.beta[c] : 0.f;
+    const int64_t gc = p.affine_period ? c % p.affine_period : c;
+    const float g = p.gamma ? p.gamma[gc] : 1.f;
+    const float bt = p.beta ? p.beta[gc] : 0.f;
     *coef = make_float4(s.mean, p.scale * g * rstd, p.scale * bt, 0.f);
     if (first) {
       if (p.save_mean) p.save_mean[c] = s.mean;

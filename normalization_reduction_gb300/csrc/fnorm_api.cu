@@ -647,7 +647,7 @@ fnorm_status in_call(const char* name, const void* x, void* y, const float* gamm
   const CallRange range(name);
   if (injected_launch_failure()) return FNORM_ERR_CUDA;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (workspace && tin == 0 && tout == 0 && !gamma && !beta && in_ws_shape(NC, S) &&
+  if (workspace && tin == 0 && tout == 0 && in_ws_shape(NC, S) &&
       aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_PATH") &&
       !env("FNORM_FORCE_SCALAR")) {
     const BnLayout l = bn_layout(1, NC, S);
@@ -660,8 +660,9 @@ fnorm_status in_call(const char* name, const void* x, void* y, const float* gamm
     unsigned* err = err_word();
     if (!err) return FNORM_ERR_CUDA;
     BnParams p{};
-    bn_fill(&p, static_cast<const float*>(x), static_cast<float*>(y), nullptr, nullptr, 1.f,
+    bn_fill(&p, static_cast<const float*>(x), static_cast<float*>(y), gamma, beta, 1.f,
             nullptr, nullptr, 0.f, eps, mean_out, rstd_out, 1, NC, S, err);
+    p.affine_period = C;
     if (p.vec && p.split) {
       p.partials = static_cast<float4*>(workspace);
       p.stats = p.partials;
@@ -692,14 +693,15 @@ fnorm_status in_call(const char* name, const void* x, void* y, const float* gamm
   // writes the result back into every one of those slots; the apply CTA of
   // each unit reads its own slot before it overwrites its range with outputs.
   // No CTA writes bytes another CTA still has to read.
-  if (!workspace && tin == 0 && tout == 0 && !gamma && !beta && x != y && in_ws_shape(NC, S) &&
+  if (!workspace && tin == 0 && tout == 0 && x != y && in_ws_shape(NC, S) &&
       aligned(x, 16) && aligned(y, 16) && S % 4 == 0 && !env("FNORM_FORCE_PATH") &&
       !env("FNORM_FORCE_SCALAR")) {
     unsigned* err = err_word();
     if (!err) return FNORM_ERR_CUDA;
     BnParams p{};
-    bn_fill(&p, static_cast<const float*>(x), static_cast<float*>(y), nullptr, nullptr, 1.f,
+    bn_fill(&p, static_cast<const float*>(x), static_cast<float*>(y), gamma, beta, 1.f,
             nullptr, nullptr, 0.f, eps, mean_out, rstd_out, 1, NC, S, err);
+    p.affine_period = C;
     if (p.vec && p.split) {
       if (env("FNORM_DEBUG_PLAN"))
         std::fprintf(stderr, "fnorm_instancenorm plan: route=output_scratch NC=%lld S=%lld units=%lld\n",

@@ -167,6 +167,9 @@ struct BnParams {
   int64_t local_kstride;
   int64_t local_copies;
   int64_t stats_kstride;
+  // gamma/beta index of BatchNorm channel c: c % affine_period (InstanceNorm
+  // as a BatchNorm over [1, N*C, S]: slice q takes gamma[q % C]); 0: c
+  int64_t affine_period;
   unsigned* grid_counter;  // resident kernel: grid-barrier arrivals (zeroed before the launch)
   bool vec;
   bool split;           // statistics pass by the register + TMA-staged kernel (vector mode)

@@ -394,6 +394,38 @@ def test_long_slices_without_workspace(orc, fnorm_env, capfd, shape):
     assert_close(xi.cpu().numpy().reshape(N * C, S), ref, torch.float32, f"in place {shape}")
 
 
+@pytest.mark.parametrize("shape", [(1, 3, 2048, 2048), (8, 3, 1024, 1024), (2, 1, 1000, 1004)])
+def test_long_slices_affine_without_workspace(orc, fnorm_env, capfd, shape):
+    """The affine form on few long fp32 slices takes the same three-launch
+    route (gamma/beta of slice q = n*C + c are those of channel c): against
+    the oracle's affine InstanceNorm, with the statistics outputs; in place it
+    takes the cluster stream and matches too."""
+    N, C = shape[0], shape[1]
+    S = int(np.prod(shape[2:]))
+    fnorm_env.setenv("FNORM_DEBUG_PLAN", "1")
+    x = inputs.normal((N, C, S), 1701 + C, dev(), mean=1.0, std=0.5)
+    gamma, beta = inputs.channel_affine(C, 1702, dev())
+    y = torch.full_like(x, float("nan"))
+    mean = torch.empty(N * C, device=dev())
+    rstd = torch.empty(N * C, device=dev())
+    fn.fnorm_instancenorm_affine(x, y, gamma, beta, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS,
+                                 mean, rstd)
+    torch.cuda.synchronize()
+    assert "route=output_scratch" in capfd.readouterr().err
+    ref, rmean, rvar = orc.instancenorm_affine(x.cpu().numpy().astype(np.float64),
+                                               gamma.cpu().numpy(), beta.cpu().numpy(), EPS)
+    assert_close(y.cpu().numpy(), ref, torch.float32, f"affine no ws {shape}")
+    assert np.max(np.abs(mean.cpu().numpy() - np.asarray(rmean).reshape(-1))) <= 1e-5
+    assert np.allclose(rstd.cpu().numpy(), 1 / np.sqrt(np.asarray(rvar).reshape(-1) + EPS),
+                       rtol=2e-6, atol=0)
+    xi = x.clone()
+    fn.fnorm_instancenorm_affine(xi, xi, gamma, beta, N, C, S, fn.FNORM_F32, fn.FNORM_F32, EPS,
+                                 None, None)
+    torch.cuda.synchronize()
+    assert "route=output_scratch" not in capfd.readouterr().err
+    assert_close(xi.cpu().numpy(), ref, torch.float32, f"affine in place {shape}")
+
+
 def test_injected_launch_failure_leaves_outputs_untouched(orc):
     """A call failed by fnorm_debug_fail_launches raises FNORM_ERR_CUDA and
     writes nothing; the next call runs normally."""
