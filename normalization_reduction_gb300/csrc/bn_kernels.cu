@@ -575,7 +575,20 @@ __global__ void __launch_bounds__(THREADS) bn_merge_kernel(const BnParams p) {
   pdl_wait();
   const float4* part = p.stats + c * p.stats_cstride;
   Stat acc = stat_empty();
-  for (int64_t i = threadIdx.x; i < p.stats_count; i += THREADS) {
+  // four loads in flight per thread before they are merged, in the same order
+  // as one at a time (the partials may lie 64 KiB apart, each its own sector):
+  // x[1,1,8192,8192] through the output-scratch route 3704-3780 -> 3961-3964
+  // GB/s, through the workspace 3999-4014 -> 4073-4103 (eight: no better)
+  constexpr int B = 4;
+  int64_t i = threadIdx.x;
+  for (; i + (B - 1) * THREADS < p.stats_count; i += B * THREADS) {
+    float4 v[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) v[b] = part[(i + b * THREADS) * p.stats_istride];
+#pragma unroll
+    for (int b = 0; b < B; ++b) acc = chan_merge(acc, Stat{v[b].x, v[b].y, v[b].z});
+  }
+  for (; i < p.stats_count; i += THREADS) {
     const float4 v = part[i * p.stats_istride];
     acc = chan_merge(acc, Stat{v.x, v.y, v.z});
   }
